@@ -1,0 +1,173 @@
+"""Seeded synthetic inputs for the five reference workloads and for tests.
+
+This module only draws random numbers (numpy ``default_rng``) and casts them to
+the tensor types; it holds none of the operators' arithmetic.  The same host
+arrays feed the CPU oracle and the CUDA path, so both see identical bits.
+
+Workloads (shapes, distributions and attributes of the operators' typical
+uses named on the pages: LLM residual stream, Mamba2 per-head gated norm,
+diffusion-UNet group norm).  ``N(m, s)`` means mean ``m`` and standard
+deviation ``s``.
+
+  ssln_fp32_64x768     SkipSimplifiedLayerNormalization fp32, input/skip
+                       (64, 768) N(0,1), bias N(0,0.1), gamma U(0.5,1.5),
+                       eps float32(1e-12), S requested; seed 0.
+  ssln_fp16_8x2048x4096  SkipSimplifiedLayerNormalization fp16, input/skip
+                       (8, 2048, 4096) N(0,1), bias N(0,0.1), gamma N(1,0.1),
+                       eps float32(1e-12), S requested; seed 1.
+  gated_fp16_4x4096x8192_c128  GatedRMSNorm fp16, X/gate (4, 4096, 8192)
+                       N(0,1), scale (128) N(1,0.1), eps 1e-5; seed 2.
+  sgn_nhwc_fp16_2x64x64x320  SkipGroupNorm channels_last, X fp16
+                       (2, 64, 64, 320) N(0,1), skip (2, 320) N(0,1), bias
+                       N(0,0.1), gamma/beta fp32 N(1,0.1)/N(0,0.1), groups 32,
+                       eps 1e-5, SiLU, S requested; seed 3.
+  sgn_nchw_fp32_16x1280x16x16  SkipGroupNorm NCHW, X fp32 (16, 1280, 16, 16)
+                       N(0,2), full skip N(0,1), no bias, gamma/beta fp16
+                       N(1,0.1)/N(0,0.1), groups 32, eps 1e-5, no activation,
+                       no S; seed 4.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+SSLN_EPS = 9.999999960041972e-13  # float32(1e-12)
+
+WORKLOADS = {
+    "ssln_fp32_64x768": dict(
+        op="skip_rms", seed=0, dtype=np.float32, shape=(64, 768), bias=True,
+        gamma=("uniform", 0.5, 1.5), epsilon=SSLN_EPS, want_sum=True),
+    "ssln_fp16_8x2048x4096": dict(
+        op="skip_rms", seed=1, dtype=np.float16, shape=(8, 2048, 4096), bias=True,
+        gamma=("normal", 1.0, 0.1), epsilon=SSLN_EPS, want_sum=True),
+    "gated_fp16_4x4096x8192_c128": dict(
+        op="gated_rms", seed=2, dtype=np.float16, shape=(4, 4096, 8192), C=128,
+        epsilon=1e-5),
+    "sgn_nhwc_fp16_2x64x64x320": dict(
+        op="skip_group", seed=3, dtype=np.float16, mdtype=np.float32,
+        shape=(2, 64, 64, 320), channels_last=1, skip="nc", bias=True, x_std=1.0,
+        groups=32, epsilon=1e-5, activation=1, want_sum=True),
+    "sgn_nchw_fp32_16x1280x16x16": dict(
+        op="skip_group", seed=4, dtype=np.float32, mdtype=np.float16,
+        shape=(16, 1280, 16, 16), channels_last=0, skip="full", bias=False, x_std=2.0,
+        groups=32, epsilon=1e-5, activation=0, want_sum=False),
+}
+
+# Order the five workloads are listed in (small SSLN first).
+WORKLOAD_ORDER = list(WORKLOADS)
+
+
+def _normal(rng, shape, mean, std, dtype):
+    z = rng.standard_normal(shape, dtype=np.float32)
+    if std != 1.0:
+        z *= np.float32(std)
+    if mean != 0.0:
+        z += np.float32(mean)
+    return z.astype(dtype, copy=False)
+
+
+def _uniform(rng, shape, lo, hi, dtype):
+    return rng.uniform(lo, hi, size=shape).astype(dtype)
+
+
+def _draw(rng, spec, shape, dtype):
+    kind, a, b = spec
+    if kind == "normal":
+        return _normal(rng, shape, a, b, dtype)
+    return _uniform(rng, shape, a, b, dtype)
+
+
+def skip_rms_inputs(shape, dtype, seed, bias=True, gamma=("normal", 1.0, 0.1),
+                    x_std=1.0):
+    """input, skip ~ N(0, x_std); bias ~ N(0, 0.1); gamma per ``gamma``."""
+    rng = np.random.default_rng(seed)
+    hidden = shape[-1]
+    x = _normal(rng, shape, 0.0, x_std, dtype)
+    sk = _normal(rng, shape, 0.0, x_std, dtype)
+    b = _normal(rng, (hidden,), 0.0, 0.1, dtype) if bias else None
+    g = _draw(rng, gamma, (hidden,), dtype)
+    return dict(input=x, skip=sk, gamma=g, bias=b)
+
+
+def gated_rms_inputs(shape, C, dtype, seed, x_std=1.0):
+    """X, gate ~ N(0, x_std); scale (C) ~ N(1, 0.1)."""
+    rng = np.random.default_rng(seed)
+    x = _normal(rng, shape, 0.0, x_std, dtype)
+    g = _normal(rng, shape, 0.0, x_std, dtype)
+    sc = _normal(rng, (C,), 1.0, 0.1, dtype)
+    return dict(x=x, gate=g, scale=sc)
+
+
+def skip_group_inputs(shape, dtype, mdtype, seed, channels_last=1, skip="full",
+                      bias=True, x_std=1.0, x_mean=0.0):
+    """X ~ N(x_mean, x_std); skip ~ N(0,1) full, (N,C) or (N,1,1,C); bias ~
+    N(0,0.1); gamma ~ N(1,0.1), beta ~ N(0,0.1) of type ``mdtype``."""
+    rng = np.random.default_rng(seed)
+    if channels_last:
+        N, H, W, C = shape
+    else:
+        N, C, H, W = shape
+    x = _normal(rng, shape, x_mean, x_std, dtype)
+    if skip == "full":
+        sk = _normal(rng, shape, 0.0, 1.0, dtype)
+    elif skip == "nc":
+        sk = _normal(rng, (N, C), 0.0, 1.0, dtype)
+    elif skip == "n11c":
+        sk = _normal(rng, (N, 1, 1, C), 0.0, 1.0, dtype)
+    else:
+        raise ValueError(skip)
+    b = _normal(rng, (C,), 0.0, 0.1, dtype) if bias else None
+    ga = _normal(rng, (C,), 1.0, 0.1, mdtype)
+    be = _normal(rng, (C,), 0.0, 0.1, mdtype)
+    return dict(x=x, skip=sk, gamma=ga, beta=be, bias=b)
+
+
+def workload(name, seed=None):
+    """Inputs and attributes of one named workload: ``(spec, arrays)``."""
+    spec = dict(WORKLOADS[name])
+    s = spec["seed"] if seed is None else seed
+    if spec["op"] == "skip_rms":
+        arrays = skip_rms_inputs(spec["shape"], spec["dtype"], s, bias=spec["bias"],
+                                 gamma=spec["gamma"])
+    elif spec["op"] == "gated_rms":
+        arrays = gated_rms_inputs(spec["shape"], spec["C"], spec["dtype"], s)
+    else:
+        arrays = skip_group_inputs(spec["shape"], spec["dtype"], spec["mdtype"], s,
+                                   channels_last=spec["channels_last"], skip=spec["skip"],
+                                   bias=spec["bias"], x_std=spec["x_std"])
+    return spec, arrays
+
+
+def algorithmic_bytes(name) -> int:
+    """Bytes that must be read plus written by one call on the workload:
+    every input element read once, every requested output written once."""
+    spec = WORKLOADS[name]
+    it = np.dtype(spec["dtype"]).itemsize
+    numel = int(np.prod(spec["shape"]))
+    if spec["op"] == "skip_rms":
+        hidden = spec["shape"][-1]
+        rd = 2 * numel * it + hidden * it * (2 if spec["bias"] else 1)
+        wr = numel * it * (2 if spec["want_sum"] else 1)
+        return rd + wr
+    if spec["op"] == "gated_rms":
+        return 2 * numel * it + spec["C"] * it + numel * it
+    if spec["channels_last"]:
+        N, H, W, C = spec["shape"]
+    else:
+        N, C, H, W = spec["shape"]
+    mit = np.dtype(spec["mdtype"]).itemsize
+    skip_n = numel if spec["skip"] == "full" else N * C
+    rd = numel * it + skip_n * it + (C * it if spec["bias"] else 0) + 2 * C * mit
+    wr = numel * it * (2 if spec["want_sum"] else 1)
+    return rd + wr
+
+
+def units(name) -> int:
+    """Rows (SSLN), C-spans (GatedRMSNorm) or group instances N*groups
+    (SkipGroupNorm) processed by one call."""
+    spec = WORKLOADS[name]
+    numel = int(np.prod(spec["shape"]))
+    if spec["op"] == "skip_rms":
+        return numel // spec["shape"][-1]
+    if spec["op"] == "gated_rms":
+        return numel // spec["C"]
+    return spec["shape"][0] * spec["groups"]
