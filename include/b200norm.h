@@ -1,0 +1,207 @@
+/*
+ * b200norm.h -- C ABI of the fused residual-add + normalization kernels for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Operators (ONNX Runtime contrib operators, as described by the README pages
+ * of the webgpu-kernels packages):
+ *   b200norm_skip_rms    com.microsoft.SkipSimplifiedLayerNormalization
+ *   b200norm_gated_rms   com.microsoft.GatedRMSNorm
+ *   b200norm_skip_group  com.microsoft.SkipGroupNorm
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer to a dense, contiguous,
+ *     row-major tensor owned by the caller.  The library never allocates,
+ *     frees or synchronises; it only enqueues kernels on `stream`.
+ *   - Pointers need only be aligned to their element size.  16-byte aligned
+ *     pointers (with spans that are whole 16-byte vectors) take the vector
+ *     path; anything else takes a scalar path with identical results.
+ *   - Element types: B200NORM_F32 (IEEE binary32) or B200NORM_F16 (IEEE
+ *     binary16).  bfloat16 is not supported (GatedRMSNorm README,
+ *     Description; the type constraints of all three pages list float32 and
+ *     float16 only).
+ *   - Rounding: the residual sum S is formed in binary32 as
+ *     (x + skip) + bias -- no add at all when bias is NULL -- and rounded once
+ *     to nearest-even at the tensor type; statistics are taken over that
+ *     rounded S (SkipGroupNorm README, Description).  Every later
+ *     intermediate is binary32; only the final store narrows to T.
+ *   - Outputs must not overlap any input or each other
+ *     (B200NORM_ERR_INVALID_ARGUMENT).
+ *   - Argument errors are reported before anything is enqueued.  Launch
+ *     failures return B200NORM_ERR_CUDA.  A call on empty tensors returns
+ *     B200NORM_OK and enqueues nothing.
+ *   - b200norm_last_error() returns a thread-local, human-readable reason for
+ *     the last non-OK status returned on the calling thread.
+ *   - Calls are stateless apart from the caller-provided SkipGroupNorm
+ *     workspace, and may be issued from several host threads at once.
+ */
+#ifndef B200NORM_H
+#define B200NORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define B200NORM_API __attribute__((visibility("default")))
+#else
+#define B200NORM_API
+#endif
+
+/* Same object as cudaStream_t (declared here so that this header does not
+ * need the CUDA headers).  NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* b200norm_stream_t;
+
+typedef enum {
+    B200NORM_F32 = 0,
+    B200NORM_F16 = 1
+} b200norm_dtype;
+
+typedef enum {
+    B200NORM_OK = 0,
+    B200NORM_ERR_INVALID_ARGUMENT = 1, /* bad pointer, shape, attribute or overlap   */
+    B200NORM_ERR_UNSUPPORTED = 2,      /* element type or shape this build refuses    */
+    B200NORM_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed        */
+    B200NORM_ERR_WORKSPACE = 4,        /* SkipGroupNorm workspace missing / too small */
+    B200NORM_ERR_DEVICE_TIMEOUT = 5    /* a device-side wait gave up (see below)      */
+} b200norm_status;
+
+/* Contract version of this ABI (1). */
+B200NORM_API int b200norm_version(void);
+
+/* Static string naming a status code. */
+B200NORM_API const char* b200norm_status_string(b200norm_status status);
+
+/* Reason for the last non-OK status returned on the calling thread ("" if
+ * none).  The pointer stays valid until the next call on this thread. */
+B200NORM_API const char* b200norm_last_error(void);
+
+/*
+ * SkipSimplifiedLayerNormalization
+ * (com.microsoft.SkipSimplifiedLayerNormalization README: Description,
+ * Inputs, Outputs, Attributes):
+ *
+ *   S[r, j]      = round_T((input[r, j] + skip[r, j]) + bias[j])
+ *   output[r, j] = round_T(S[r, j] * (1 / sqrt(mean_j(S[r, :]^2) + epsilon)) * gamma[j])
+ *
+ *   input, skip          T, (rows, hidden), row-major.  rows is the product of
+ *                        the leading axes: (token_count) or (batch * sequence).
+ *   gamma                T, (hidden).
+ *   bias                 T, (hidden), or NULL when absent.
+ *   output               T, (rows, hidden).
+ *   input_skip_bias_sum  T, (rows, hidden): receives S; NULL when not requested.
+ *   epsilon              >= 0 and not NaN; the operator default is
+ *                        9.999999960041972e-13 (float32 of 1e-12).
+ *
+ * rows == 0 is a no-op.  hidden must be > 0.
+ */
+B200NORM_API b200norm_status b200norm_skip_rms(const void* input, const void* skip,
+                                               const void* gamma, const void* bias, void* output,
+                                               void* input_skip_bias_sum, int64_t rows,
+                                               int64_t hidden, b200norm_dtype T, float epsilon,
+                                               b200norm_stream_t stream);
+
+/*
+ * Same as b200norm_skip_rms, and also writes the per-row statistics outputs
+ * that the operator schema lists (SkipSimplifiedLayerNormalization README,
+ * Outputs: mean, inv_std_var, element type U = float32, shape of the input
+ * with the last axis replaced by 1):
+ *   mean[r]        = 0 (the simplified form does not centre the row)
+ *   inv_std_var[r] = 1 / sqrt(mean_j(S[r, :]^2) + epsilon)
+ * Either pointer may be NULL.  Both are float32 device arrays of `rows`.
+ */
+B200NORM_API b200norm_status b200norm_skip_rms_stats(const void* input, const void* skip,
+                                                     const void* gamma, const void* bias,
+                                                     void* output, void* input_skip_bias_sum,
+                                                     float* mean, float* inv_std_var,
+                                                     int64_t rows, int64_t hidden,
+                                                     b200norm_dtype T, float epsilon,
+                                                     b200norm_stream_t stream);
+
+/*
+ * GatedRMSNorm (com.microsoft.GatedRMSNorm README: Description, Inputs,
+ * Attributes):
+ *
+ *   for each contiguous span r of C elements (rows = numel / C):
+ *   y[r, j] = round_T(x[r, j] * (1 / sqrt(mean_j(x[r, :]^2) + epsilon))
+ *                     * scale[j] * SiLU(gate[r, j])),   SiLU(g) = g / (1 + e^-g)
+ *
+ *   x, gate, y   T, numel elements (any rank >= 1, folded to (numel / C, C)).
+ *   scale        T, C elements: (C), (1, C) and (C, 1) are the same vector.
+ *   numel        must be a multiple of C; numel == 0 is a no-op.
+ *   C            > 0.
+ *   epsilon      >= 0 and not NaN; operator default 1e-5.
+ *
+ * Every intermediate, SiLU included, is binary32.
+ */
+B200NORM_API b200norm_status b200norm_gated_rms(const void* x, const void* gate,
+                                                const void* scale, void* y, int64_t numel,
+                                                int64_t C, b200norm_dtype T, float epsilon,
+                                                b200norm_stream_t stream);
+
+/*
+ * SkipGroupNorm (com.microsoft.SkipGroupNorm README: Description, Inputs,
+ * Outputs, Attributes, Type constraints):
+ *
+ *   S = round_T((X + skip) + bias)                          (bias may be NULL)
+ *   Y = round_T(act((S - mean) * rstd * gamma[c] + beta[c])), evaluated in
+ *       binary32, rstd = 1 / sqrt(var + epsilon), act = SiLU (z / (1 + e^-z))
+ *       when activation == 1, identity when 0.
+ *   mean and var (population) are taken per batch item n and group g over the
+ *   C / groups channels of g and every spatial position.
+ *
+ *   x, y, s   T.  Physical layout (N, H, W, C) when channels_last != 0, else
+ *             (N, C, H, W).  N, C, H, W below are the LOGICAL sizes.
+ *   skip      T.  skip_rank / skip_dims give its shape:
+ *               - exactly x's physical shape                     full skip;
+ *               - (N, C) or (N, 1, 1, C)       one value per (n, c), at
+ *                                              offset n * C + c, both layouts.
+ *             A (N, 1, 1, C) skip when H == W == 1 is an exact match and takes
+ *             the full route (same offsets, same results).
+ *   bias      T, (C), or NULL.
+ *   gamma, beta  M, (C).  M is independent of T.
+ *   s         receives S when not NULL.
+ *   groups    > 0 and must divide C.
+ *   activation  0 (none) or 1 (SiLU); required.
+ *   epsilon   >= 0 and not NaN; operator default 1e-5.
+ *   workspace device memory of at least
+ *             b200norm_skip_group_workspace_size(...) bytes, 256-byte aligned,
+ *             ZERO-FILLED before its first use (b200norm_workspace_init does
+ *             that).  A call that completes normally leaves it ready for the
+ *             next call.  Calls that share a workspace must not overlap on the
+ *             device (enqueue them on one stream).
+ *
+ * Cross-CTA waits inside the kernels are bounded: a wait that does not
+ * complete within about one second makes the kernel record
+ * B200NORM_ERR_DEVICE_TIMEOUT in the workspace and return early (outputs are
+ * then undefined).  b200norm_workspace_status() reads that record.
+ */
+B200NORM_API size_t b200norm_skip_group_workspace_size(int64_t N, int64_t C, int64_t H,
+                                                       int64_t W, int groups, b200norm_dtype T,
+                                                       int channels_last);
+
+B200NORM_API b200norm_status b200norm_skip_group(
+    const void* x, const void* skip, int skip_rank, const int64_t* skip_dims, const void* bias,
+    const void* gamma, const void* beta, void* y, void* s, int64_t N, int64_t C, int64_t H,
+    int64_t W, b200norm_dtype T, b200norm_dtype M, int groups, float epsilon, int activation,
+    int channels_last, void* workspace, size_t workspace_bytes, b200norm_stream_t stream);
+
+/* Zero-fill a SkipGroupNorm workspace (cudaMemsetAsync on `stream`). */
+B200NORM_API b200norm_status b200norm_workspace_init(void* workspace, size_t workspace_bytes,
+                                                     b200norm_stream_t stream);
+
+/* Synchronise `stream`, then read the workspace's device-side error record:
+ * B200NORM_OK, or B200NORM_ERR_DEVICE_TIMEOUT if a bounded wait gave up (the
+ * workspace must then be re-initialised).  B200NORM_ERR_CUDA if the copy
+ * failed. */
+B200NORM_API b200norm_status b200norm_workspace_status(const void* workspace,
+                                                       b200norm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* B200NORM_H */

@@ -1,0 +1,47 @@
+/*
+ * b200norm_testing.h -- hooks for the library's own tests.  Not needed to use
+ * the operators; they let tests reach every schedule and the device-side
+ * timeout path without faulting or hanging a GPU.
+ */
+#ifndef B200NORM_TESTING_H
+#define B200NORM_TESTING_H
+
+#include "b200norm.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Launch a two-CTA cooperative kernel whose grid barrier can never complete
+ * (it waits for a third CTA).  Both CTAs give up after `limit_ns`
+ * nanoseconds and record B200NORM_ERR_DEVICE_TIMEOUT in the workspace, which
+ * b200norm_workspace_status() then reports.  The workspace must be
+ * re-initialised afterwards.  Never faults; returns within ~limit_ns. */
+B200NORM_API b200norm_status b200norm_testing_barrier_timeout(void* workspace,
+                                                              size_t workspace_bytes,
+                                                              uint64_t limit_ns,
+                                                              b200norm_stream_t stream);
+
+/* Force a schedule on the calling thread (0 = automatic choice):
+ *   row_mode:    2 = walk each row twice (any row length)
+ *   group_route: 3 = two-phase partials -> normalize (any shape)
+ * Other values are rejected with B200NORM_ERR_INVALID_ARGUMENT. */
+B200NORM_API b200norm_status b200norm_testing_force(int row_mode, int group_route);
+
+/* Schedule the automatic planner picks, without launching anything.
+ * Rows (SSLN / GatedRMSNorm): out = {mode, ve, tpr, nv, rpg, block, csize, grid}.
+ * SkipGroupNorm: out = {route, ve, nv, block, csize, grid, ctas_per_item,
+ * pix_per_cta}.  `aligned16` says whether every pointer is 16-byte aligned. */
+B200NORM_API b200norm_status b200norm_testing_plan_rows(int64_t rows, int64_t n,
+                                                        b200norm_dtype T, int aligned16,
+                                                        int64_t out[8]);
+B200NORM_API b200norm_status b200norm_testing_plan_group(int64_t N, int64_t C, int64_t H,
+                                                         int64_t W, int groups, b200norm_dtype T,
+                                                         b200norm_dtype M, int channels_last,
+                                                         int aligned16, int64_t out[8]);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* B200NORM_TESTING_H */

@@ -1,0 +1,243 @@
+// common.cuh -- device helpers shared by the b200norm kernels (sm_103a).
+//
+// Vector I/O with cache hints, element conversions, warp / CTA / cluster
+// reductions (cluster partials exchanged through distributed shared memory),
+// Chan's pairwise merge of (count, mean, M2) moments, and a bounded
+// grid-wide barrier for cooperative launches.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace b200norm {
+
+// ---------------------------------------------------------------------------
+// Element types
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) {
+  return __float2half_rn(v);  // round to nearest-even, subnormals kept
+}
+
+// A pack of N elements of T moved as one access of sizeof(T) * N bytes.
+template <typename T, int N>
+struct alignas(sizeof(T) * N) Pack {
+  T v[N];
+};
+
+template <int BYTES> struct RawOf;
+template <> struct RawOf<16> { using type = uint4; };
+template <> struct RawOf<8> { using type = uint2; };
+template <> struct RawOf<4> { using type = unsigned int; };
+template <> struct RawOf<2> { using type = unsigned short; };
+
+// Streaming load: data read exactly once (evict-first in L1 and L2).
+template <typename T, int N>
+__device__ __forceinline__ Pack<T, N> ld_stream(const T* p) {
+  using R = typename RawOf<sizeof(T) * N>::type;
+  R r = __ldcs(reinterpret_cast<const R*>(p));
+  Pack<T, N> out;
+  memcpy(&out, &r, sizeof(R));
+  return out;
+}
+
+// Read-only load of data reused by many CTAs (weights, biases).
+template <typename T, int N>
+__device__ __forceinline__ Pack<T, N> ld_reuse(const T* p) {
+  using R = typename RawOf<sizeof(T) * N>::type;
+  R r = __ldg(reinterpret_cast<const R*>(p));
+  Pack<T, N> out;
+  memcpy(&out, &r, sizeof(R));
+  return out;
+}
+
+// Streaming store (evict-first).
+template <typename T, int N>
+__device__ __forceinline__ void st_stream(T* p, const Pack<T, N>& v) {
+  using R = typename RawOf<sizeof(T) * N>::type;
+  R r;
+  memcpy(&r, &v, sizeof(R));
+  __stcs(reinterpret_cast<R*>(p), r);
+}
+
+// The residual sum at type T: binary32 (x + skip), then + bias when present,
+// then one rounding to T.
+template <typename T, bool HAS_BIAS>
+__device__ __forceinline__ T residual_sum(T x, T skip, T bias) {
+  float t = __fadd_rn(to_f32(x), to_f32(skip));
+  if constexpr (HAS_BIAS) t = __fadd_rn(t, to_f32(bias));
+  return from_f32<T>(t);
+}
+
+// SiLU in binary32: z * sigmoid(z) = z / (1 + e^-z).  Uses the fast exp and
+// divide intrinsics (a few ulp of binary32, far inside the output tolerance).
+__device__ __forceinline__ float silu_f32(float z) {
+  return __fdividef(z, 1.0f + __expf(-z));
+}
+
+// ---------------------------------------------------------------------------
+// Reductions
+// ---------------------------------------------------------------------------
+// Butterfly sum over aligned segments of `width` lanes (width a power of two
+// <= 32).  Every lane of a segment ends with the bitwise-identical total
+// (each step adds the same two operands on both partners).
+__device__ __forceinline__ float seg_sum(float v, int width) {
+  for (int o = width >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sum over the whole CTA; every thread returns the same value.  `red` is a
+// shared array of at least 33 floats.  Fixed association order.
+__device__ __forceinline__ float cta_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    float t = lane < nwarps ? red[lane] : 0.0f;
+    t = warp_sum(t);
+    if (lane == 0) red[32] = t;
+  }
+  __syncthreads();
+  return red[32];
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters (distributed shared memory)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ unsigned cluster_size() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+// Hardware cluster barrier: every thread of every CTA of the cluster arrives;
+// release/acquire make shared (and global) writes before it visible after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Load a float that CTA `rank` of this cluster holds at the same shared
+// address as `local` does here.
+__device__ __forceinline__ float ld_cluster_f32(const float* local, unsigned rank) {
+  unsigned addr = static_cast<unsigned>(__cvta_generic_to_shared(local));
+  unsigned remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// Sum of one value per CTA over the cluster, in rank order (identical in every
+// CTA).  `slot` is a shared float reserved for this call; the caller must
+// cluster_sync() once more before any CTA of the cluster exits.
+__device__ __forceinline__ float cluster_sum(float cta_value, float* slot, unsigned csize) {
+  if (threadIdx.x == 0) *slot = cta_value;
+  cluster_sync();
+  float t = 0.0f;
+  for (unsigned r = 0; r < csize; ++r) t += ld_cluster_f32(slot, r);
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// Moments: Chan et al.'s pairwise update of (count, mean, M2), M2 = sum of
+// squared deviations from the mean.
+// ---------------------------------------------------------------------------
+struct Moments {
+  float n, mean, m2;
+};
+
+__device__ __forceinline__ Moments merge(Moments a, Moments b) {
+  if (b.n == 0.0f) return a;
+  if (a.n == 0.0f) return b;
+  const float n = a.n + b.n;
+  const float d = b.mean - a.mean;
+  const float fb = b.n / n;
+  Moments r;
+  r.n = n;
+  r.mean = a.mean + d * fb;
+  r.m2 = a.m2 + b.m2 + d * d * a.n * fb;
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Bounded grid barrier (cooperative launches only: every CTA is resident).
+// ---------------------------------------------------------------------------
+// Control block at the start of a SkipGroupNorm workspace.
+struct Control {
+  unsigned int bar_count;  // CTAs arrived at the current barrier (0 between barriers)
+  unsigned int bar_gen;    // barrier generation
+  unsigned int error;      // 0, or a b200norm_status recorded by a kernel
+  unsigned int error_site; // which wait gave up
+};
+
+constexpr unsigned kStatusDeviceTimeout = 5;  // B200NORM_ERR_DEVICE_TIMEOUT
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// All `expected` CTAs of the grid call this once per barrier.  The last CTA to
+// arrive resets the count and bumps the generation, so the control block is
+// left ready for the next barrier or call.  A CTA that waits longer than
+// `limit_ns` records a timeout and returns false; the caller must then stop.
+__device__ __forceinline__ bool grid_barrier(Control* ctl, unsigned expected,
+                                             unsigned long long limit_ns, unsigned site) {
+  __shared__ int ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned gen = ld_acquire_gpu(&ctl->bar_gen);
+    __threadfence();
+    const unsigned arrived = atomicAdd(&ctl->bar_count, 1u) + 1u;
+    ok = 1;
+    if (arrived == expected) {
+      atomicExch(&ctl->bar_count, 0u);
+      __threadfence();
+      atomicAdd(&ctl->bar_gen, 1u);
+    } else {
+      const unsigned long long t0 = global_ns();
+      while (ld_acquire_gpu(&ctl->bar_gen) == gen) {
+        if (global_ns() - t0 > limit_ns) {
+          atomicExch(&ctl->error, kStatusDeviceTimeout);
+          atomicExch(&ctl->error_site, site);
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  return ok != 0;
+}
+
+}  // namespace b200norm

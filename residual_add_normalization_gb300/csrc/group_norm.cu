@@ -1,0 +1,803 @@
+// group_norm.cu -- SkipGroupNorm kernels (sm_103a).
+//
+// S = round_T((X + skip) + bias); Y = round_T(act((S - mean) * rstd * gamma[c] + beta[c]))
+// with mean / population variance per (batch item n, group g) over the C/groups
+// channels of g and every spatial position (com.microsoft.SkipGroupNorm README,
+// Description).  Three routes:
+//
+//   1. NCHW resident.  A group instance (n, g) is one contiguous run of
+//      cpg * H * W elements.  One CTA -- or a cluster of up to 16 CTAs for
+//      long runs -- holds the whole run in registers: one HBM read, exact
+//      two-pass (centred) statistics from registers, one write.  Cluster
+//      partials are exchanged through distributed shared memory.
+//   2. NHWC cooperative.  A group's elements are strided through the tensor
+//      (cpg channels of every pixel), so statistics need every CTA that holds
+//      a piece of the batch item.  One cooperative grid: each CTA holds a
+//      slab of whole pixels in registers, reduces per-channel then per-group
+//      (count, mean, M2) moments with Chan's merge, publishes them, meets the
+//      other CTAs at one bounded grid barrier, merges its batch item's
+//      partials and normalizes what it holds.
+//   3. Two-phase, any shape or layout.  Kernel A forms S over fixed chunks of
+//      each group instance and writes per-chunk moments; kernel B merges them
+//      and re-forms S from the inputs to normalize (the re-read is an L2 hit
+//      for anything that fits in L2).
+//
+// Every route carries the group mean as K + d: K an exact data value of the
+// group (its first residual sum), d the mean of S - K.  S - K is exact for
+// data near the mean, so (S - K) - d stays accurate in binary32 even when
+// |mean| is large against the group's spread.
+#include "common.cuh"
+#include "launch.h"
+
+namespace b200norm {
+
+template <typename T, typename M>
+struct SgnArgs {
+  const T* __restrict__ x;
+  const T* __restrict__ skip;
+  const T* __restrict__ bias;   // may be null
+  const M* __restrict__ gamma;
+  const M* __restrict__ beta;
+  T* __restrict__ y;
+  T* __restrict__ s;            // may be null
+  int64_t N;
+  int C, HW, cpg, groups;
+  int bcast;                    // skip holds one value per (n, c)
+  int act;                      // 1: SiLU after the affine transform
+  float eps;
+  Control* ctl;                 // workspace control block
+  float4* part;                 // workspace moment slots (n, mean, M2, -)
+  unsigned long long limit_ns;  // bound of every cross-CTA wait
+};
+
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr int kResidentMaxThreads = 512;
+constexpr int kCoopMaxThreads = 512;
+constexpr int kTwoPhaseThreads = 256;
+constexpr int kTwoPhaseEpt = kTwoPhaseChunk / kTwoPhaseThreads;
+constexpr size_t kMaxSmemBytes = 227 * 1024;
+
+// S element at type T from binary32 x and skip, plus bias when present.
+template <typename T>
+__device__ __forceinline__ T sgn_sum(float x, float sk, const T* __restrict__ bias, int c) {
+  float t = __fadd_rn(x, sk);
+  if (bias) t = __fadd_rn(t, to_f32(bias[c]));
+  return from_f32<T>(t);
+}
+
+// ((S - K) - d) * rstd * gamma + beta, then SiLU when requested.
+__device__ __forceinline__ float sgn_out(float s, float K, float d, float rstd, float ga,
+                                         float be, int act) {
+  float z = ((s - K) - d) * rstd * ga + be;
+  if (act) z = silu_f32(z);
+  return z;
+}
+
+// Shift K of group instance (n, g): its residual sum at (channel g*cpg, pixel 0).
+template <typename T, typename M>
+__device__ __forceinline__ float sgn_shift(const SgnArgs<T, M>& a, int64_t n, int g, bool cl) {
+  const int c = g * a.cpg;
+  const int64_t off = cl ? n * a.HW * a.C + c : (n * a.C + c) * static_cast<int64_t>(a.HW);
+  const float sk = a.bcast ? to_f32(a.skip[n * a.C + c]) : to_f32(a.skip[off]);
+  return to_f32(sgn_sum<T>(to_f32(a.x[off]), sk, a.bias, c));
+}
+
+// ---------------------------------------------------------------------------
+// Route 1: NCHW, one CTA or cluster per group instance
+// ---------------------------------------------------------------------------
+// VE elements per access; requires H*W % VE == 0 so an access never straddles
+// two channels.  Thread t of cluster rank r holds vectors
+// t + r*blockDim + k*(blockDim*csize), k < NV.
+template <typename T, typename M, int VE, int NV>
+__global__ void __launch_bounds__(kResidentMaxThreads)
+sgn_nchw_resident(const SgnArgs<T, M> a) {
+  __shared__ float red[33];
+  __shared__ float slot_sum, slot_m2;
+  const unsigned csize = cluster_size();
+  const unsigned rank = csize > 1 ? cluster_rank() : 0u;
+  const int64_t inst = blockIdx.x / csize;
+  const int64_t n = inst / a.groups;
+  const int g = static_cast<int>(inst % a.groups);
+  const int L = a.cpg * a.HW;
+  const int nvec = L / VE;
+  const int tpr = blockDim.x * csize;
+  const int first = threadIdx.x + static_cast<int>(rank) * blockDim.x;
+  const int64_t base = (n * a.C + static_cast<int64_t>(g) * a.cpg) * a.HW;
+
+  Pack<T, VE> xv[NV], kv[NV], sv[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int v = first + k * tpr;
+    if (v < nvec) {
+      xv[k] = ld_stream<T, VE>(a.x + base + static_cast<int64_t>(v) * VE);
+      if (!a.bcast) kv[k] = ld_stream<T, VE>(a.skip + base + static_cast<int64_t>(v) * VE);
+    }
+  }
+  const float K = sgn_shift(a, n, g, false);
+  float sum = 0.0f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int v = first + k * tpr;
+    if (v < nvec) {
+      const int c = g * a.cpg + (v * VE) / a.HW;
+      const float skb = a.bcast ? to_f32(a.skip[n * a.C + c]) : 0.0f;
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        const float sk = a.bcast ? skb : to_f32(kv[k].v[e]);
+        sv[k].v[e] = sgn_sum<T>(to_f32(xv[k].v[e]), sk, a.bias, c);
+        sum += to_f32(sv[k].v[e]) - K;
+      }
+      if (a.s) st_stream<T, VE>(a.s + base + static_cast<int64_t>(v) * VE, sv[k]);
+    }
+  }
+  float tot = cta_sum(sum, red);
+  if (csize > 1) tot = cluster_sum(tot, &slot_sum, csize);
+  const float dmean = tot / static_cast<float>(L);  // mean = K + dmean
+  float m2 = 0.0f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int v = first + k * tpr;
+    if (v < nvec) {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        const float d = (to_f32(sv[k].v[e]) - K) - dmean;
+        m2 = fmaf(d, d, m2);
+      }
+    }
+  }
+  tot = cta_sum(m2, red);
+  if (csize > 1) tot = cluster_sum(tot, &slot_m2, csize);
+  const float rstd = 1.0f / sqrtf(tot / static_cast<float>(L) + a.eps);
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int v = first + k * tpr;
+    if (v < nvec) {
+      const int c = g * a.cpg + (v * VE) / a.HW;
+      const float ga = to_f32(a.gamma[c]), be = to_f32(a.beta[c]);
+      Pack<T, VE> out;
+#pragma unroll
+      for (int e = 0; e < VE; ++e)
+        out.v[e] = from_f32<T>(sgn_out(to_f32(sv[k].v[e]), K, dmean, rstd, ga, be, a.act));
+      st_stream<T, VE>(a.y + base + static_cast<int64_t>(v) * VE, out);
+    }
+  }
+  if (csize > 1) cluster_sync();  // peers may still read slot_m2
+}
+
+// ---------------------------------------------------------------------------
+// Route 2: NHWC, cooperative grid with one bounded grid barrier
+// ---------------------------------------------------------------------------
+// blockDim.x = CV * PL with CV = C / VE vectors per pixel: thread t covers the
+// VE channels (t % CV) * VE .. +VE of pixels p0 + t / CV + k * PL, k < NV.
+// CTA b handles batch item b / B, pixels [(b % B) * ppc, +ppc).
+// Dynamic shared memory (floats):
+//   phase 1: cnt[PL] | mean[PL*C] | m2[PL*C]        (per pixel lane, per channel)
+//   phase 3: part[B*groups] as float4, then gmean[groups] | grstd[groups]
+//   tail at k_offset (after the larger of the two, kept throughout): K[groups]
+// Moments are of S - K[g].
+template <typename T, typename M, int VE, int NV>
+__global__ void __launch_bounds__(kCoopMaxThreads)
+sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
+  extern __shared__ float4 smem4[];
+  float* smem = reinterpret_cast<float*>(smem4);
+  float* s_K = smem + k_offset;
+  const int C = a.C;
+  const int CV = C / VE;
+  const int PL = blockDim.x / CV;
+  const int tc = threadIdx.x % CV;
+  const int tp = threadIdx.x / CV;
+  const int n = blockIdx.x / B;
+  const int p0 = (blockIdx.x % B) * ppc;
+  const int p1 = min(p0 + ppc, a.HW);
+  const int64_t nbase = static_cast<int64_t>(n) * a.HW * C;
+  const int c0 = tc * VE;
+
+  // --- load and form S --------------------------------------------------
+  Pack<T, VE> xv[NV], kv[NV], sv[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int p = p0 + tp + k * PL;
+    if (p < p1) {
+      const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+      xv[k] = ld_stream<T, VE>(a.x + off);
+      if (!a.bcast) kv[k] = ld_stream<T, VE>(a.skip + off);
+    }
+  }
+  Pack<T, VE> skb;
+  if (a.bcast) skb = ld_reuse<T, VE>(a.skip + static_cast<int64_t>(n) * C + c0);
+  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) s_K[gg] = sgn_shift(a, n, gg, true);
+  __syncthreads();
+  float Kl[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) Kl[e] = s_K[(c0 + e) / a.cpg];
+  int cnt = 0;
+  float lsum[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) lsum[e] = 0.0f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int p = p0 + tp + k * PL;
+    if (p < p1) {
+      ++cnt;
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        const float sk = a.bcast ? to_f32(skb.v[e]) : to_f32(kv[k].v[e]);
+        sv[k].v[e] = sgn_sum<T>(to_f32(xv[k].v[e]), sk, a.bias, c0 + e);
+        lsum[e] += to_f32(sv[k].v[e]) - Kl[e];
+      }
+      if (a.s) st_stream<T, VE>(a.s + nbase + static_cast<int64_t>(p) * C + c0, sv[k]);
+    }
+  }
+  // --- per-thread exact moments of each of its channels ------------------
+  float* s_cnt = smem;
+  float* s_mean = smem + PL;
+  float* s_m2 = s_mean + PL * C;
+  const float fcnt = static_cast<float>(cnt);
+#pragma unroll
+  for (int e = 0; e < VE; ++e) {
+    const float mu = cnt ? lsum[e] / fcnt : 0.0f;
+    float m2 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int p = p0 + tp + k * PL;
+      if (p < p1) {
+        const float d = (to_f32(sv[k].v[e]) - Kl[e]) - mu;
+        m2 = fmaf(d, d, m2);
+      }
+    }
+    s_mean[tp * C + c0 + e] = mu;
+    s_m2[tp * C + c0 + e] = m2;
+  }
+  if (tc == 0) s_cnt[tp] = fcnt;
+  __syncthreads();
+  // --- merge pixel lanes per channel (tree over tp, fixed order) ----------
+  for (int stride = 1; stride < PL; stride <<= 1) {
+    for (int idx = threadIdx.x; idx < PL * C; idx += blockDim.x) {
+      const int t = idx / C, c = idx % C;
+      if ((t % (2 * stride)) == 0 && t + stride < PL) {
+        const Moments m = merge(Moments{s_cnt[t], s_mean[t * C + c], s_m2[t * C + c]},
+                                Moments{s_cnt[t + stride], s_mean[(t + stride) * C + c],
+                                        s_m2[(t + stride) * C + c]});
+        s_mean[t * C + c] = m.mean;
+        s_m2[t * C + c] = m.m2;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < PL) {
+      const int t = threadIdx.x;
+      if ((t % (2 * stride)) == 0 && t + stride < PL) s_cnt[t] += s_cnt[t + stride];
+    }
+    __syncthreads();
+  }
+  // --- merge the channels of each group, publish the CTA's moments --------
+  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
+    Moments m{0.0f, 0.0f, 0.0f};
+    for (int cc = 0; cc < a.cpg; ++cc) {
+      const int c = gg * a.cpg + cc;
+      m = merge(m, Moments{s_cnt[0], s_mean[c], s_m2[c]});
+    }
+    a.part[static_cast<int64_t>(blockIdx.x) * a.groups + gg] = make_float4(m.n, m.mean, m.m2, 0.0f);
+  }
+  __threadfence();
+  if (!grid_barrier(a.ctl, gridDim.x, a.limit_ns, 1u)) return;
+
+  // --- merge the batch item's B partials per group (tree, fixed order) ----
+  float4* s_part = smem4;
+  float* s_gmean = reinterpret_cast<float*>(s_part + static_cast<int64_t>(B) * a.groups);
+  float* s_grstd = s_gmean + a.groups;
+  const float4* src = a.part + static_cast<int64_t>(n) * B * a.groups;
+  for (int idx = threadIdx.x; idx < B * a.groups; idx += blockDim.x) s_part[idx] = __ldcg(src + idx);
+  __syncthreads();
+  for (int stride = 1; stride < B; stride <<= 1) {
+    for (int idx = threadIdx.x; idx < B * a.groups; idx += blockDim.x) {
+      const int b = idx / a.groups;
+      if ((b % (2 * stride)) == 0 && b + stride < B) {
+        const float4 u = s_part[idx], w = s_part[idx + stride * a.groups];
+        const Moments m = merge(Moments{u.x, u.y, u.z}, Moments{w.x, w.y, w.z});
+        s_part[idx] = make_float4(m.n, m.mean, m.m2, 0.0f);
+      }
+    }
+    __syncthreads();
+  }
+  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
+    const float4 u = s_part[gg];
+    s_gmean[gg] = u.y;
+    s_grstd[gg] = 1.0f / sqrtf(u.z / u.x + a.eps);
+  }
+  __syncthreads();
+  // --- normalize what this thread holds -----------------------------------
+  float ga[VE], be[VE], mu[VE], rs[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) {
+    const int c = c0 + e;
+    ga[e] = to_f32(a.gamma[c]);
+    be[e] = to_f32(a.beta[c]);
+    mu[e] = s_gmean[c / a.cpg];
+    rs[e] = s_grstd[c / a.cpg];
+  }
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int p = p0 + tp + k * PL;
+    if (p < p1) {
+      Pack<T, VE> out;
+#pragma unroll
+      for (int e = 0; e < VE; ++e)
+        out.v[e] = from_f32<T>(
+            sgn_out(to_f32(sv[k].v[e]), Kl[e], mu[e], rs[e], ga[e], be[e], a.act));
+      st_stream<T, VE>(a.y + nbase + static_cast<int64_t>(p) * C + c0, out);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Route 3: two-phase, any layout
+// ---------------------------------------------------------------------------
+// Element j of group instance (n, g), j in [0, cpg*HW):
+//   NCHW: offset (n*C + g*cpg)*HW + j,                 channel g*cpg + j / HW
+//   NHWC: offset (n*HW + j / cpg)*C + g*cpg + j % cpg,  channel g*cpg + j % cpg
+template <typename T, typename M>
+__device__ __forceinline__ void sgn_locate(const SgnArgs<T, M>& a, int64_t n, int g, int64_t j,
+                                           bool cl, int64_t* off, int* c) {
+  if (cl) {
+    const int64_t p = j / a.cpg;
+    const int cc = static_cast<int>(j % a.cpg);
+    *c = g * a.cpg + cc;
+    *off = (n * a.HW + p) * a.C + *c;
+  } else {
+    *c = g * a.cpg + static_cast<int>(j / a.HW);
+    *off = (n * a.C + static_cast<int64_t>(g) * a.cpg) * a.HW + j;
+  }
+}
+
+template <typename T, typename M>
+__device__ __forceinline__ float sgn_form(const SgnArgs<T, M>& a, int64_t n, int64_t off, int c) {
+  const float x = to_f32(__ldcs(a.x + off));
+  const float sk = a.bcast ? to_f32(a.skip[n * a.C + c]) : to_f32(__ldcs(a.skip + off));
+  return to_f32(sgn_sum<T>(x, sk, a.bias, c));
+}
+
+// Merge `count` moments held in shared memory (tree, fixed order); result in [0].
+__device__ __forceinline__ void smem_merge(float* mn, float* mm, float* m2, int count) {
+  for (int stride = 1; stride < count; stride <<= 1) {
+    for (int i = threadIdx.x; i < count; i += blockDim.x) {
+      if ((i % (2 * stride)) == 0 && i + stride < count) {
+        const Moments r = merge(Moments{mn[i], mm[i], m2[i]},
+                                Moments{mn[i + stride], mm[i + stride], m2[i + stride]});
+        mn[i] = r.n;
+        mm[i] = r.mean;
+        m2[i] = r.m2;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <typename T, typename M, bool CL>
+__global__ void __launch_bounds__(kTwoPhaseThreads)
+sgn_partials(const SgnArgs<T, M> a, int chunks) {
+  __shared__ float mn[kTwoPhaseThreads], mm[kTwoPhaseThreads], m2s[kTwoPhaseThreads];
+  const int64_t inst = blockIdx.x / chunks;
+  const int q = blockIdx.x % chunks;
+  const int64_t n = inst / a.groups;
+  const int g = static_cast<int>(inst % a.groups);
+  const int64_t L = static_cast<int64_t>(a.cpg) * a.HW;
+  const int64_t j0 = static_cast<int64_t>(q) * kTwoPhaseChunk;
+  const float K = sgn_shift(a, n, g, CL);
+  float v[kTwoPhaseEpt];
+  int cnt = 0;
+  float sum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kTwoPhaseEpt; ++i) {
+    const int64_t j = j0 + threadIdx.x + static_cast<int64_t>(i) * kTwoPhaseThreads;
+    v[i] = 0.0f;
+    if (j < L) {
+      int64_t off;
+      int c;
+      sgn_locate(a, n, g, j, CL, &off, &c);
+      const float x = to_f32(__ldcs(a.x + off));
+      const float sk = a.bcast ? to_f32(a.skip[n * a.C + c]) : to_f32(__ldcs(a.skip + off));
+      const T sT = sgn_sum<T>(x, sk, a.bias, c);
+      if (a.s) a.s[off] = sT;
+      v[i] = to_f32(sT) - K;
+      sum += v[i];
+      ++cnt;
+    }
+  }
+  const float mu = cnt ? sum / static_cast<float>(cnt) : 0.0f;
+  float m2 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kTwoPhaseEpt; ++i) {
+    const int64_t j = j0 + threadIdx.x + static_cast<int64_t>(i) * kTwoPhaseThreads;
+    if (j < L) {
+      const float d = v[i] - mu;
+      m2 = fmaf(d, d, m2);
+    }
+  }
+  mn[threadIdx.x] = static_cast<float>(cnt);
+  mm[threadIdx.x] = mu;
+  m2s[threadIdx.x] = m2;
+  __syncthreads();
+  smem_merge(mn, mm, m2s, blockDim.x);
+  if (threadIdx.x == 0) a.part[blockIdx.x] = make_float4(mn[0], mm[0], m2s[0], 0.0f);
+}
+
+template <typename T, typename M, bool CL>
+__global__ void __launch_bounds__(kTwoPhaseThreads)
+sgn_normalize(const SgnArgs<T, M> a, int chunks) {
+  __shared__ float mn[kTwoPhaseThreads], mm[kTwoPhaseThreads], m2s[kTwoPhaseThreads];
+  __shared__ float s_mean, s_rstd;
+  const int64_t inst = blockIdx.x / chunks;
+  const int q = blockIdx.x % chunks;
+  const int64_t n = inst / a.groups;
+  const int g = static_cast<int>(inst % a.groups);
+  const int64_t L = static_cast<int64_t>(a.cpg) * a.HW;
+  // merge this instance's chunk moments: each thread folds a strided subset
+  // in order, then a tree over threads
+  Moments m{0.0f, 0.0f, 0.0f};
+  for (int i = threadIdx.x; i < chunks; i += blockDim.x) {
+    const float4 u = __ldcg(a.part + inst * chunks + i);
+    m = merge(m, Moments{u.x, u.y, u.z});
+  }
+  mn[threadIdx.x] = m.n;
+  mm[threadIdx.x] = m.mean;
+  m2s[threadIdx.x] = m.m2;
+  __syncthreads();
+  smem_merge(mn, mm, m2s, blockDim.x);
+  if (threadIdx.x == 0) {
+    s_mean = mm[0];
+    s_rstd = 1.0f / sqrtf(m2s[0] / mn[0] + a.eps);
+  }
+  __syncthreads();
+  const float dmean = s_mean, rstd = s_rstd;
+  const float K = sgn_shift(a, n, g, CL);
+  const int64_t j0 = static_cast<int64_t>(q) * kTwoPhaseChunk;
+#pragma unroll 4
+  for (int i = 0; i < kTwoPhaseEpt; ++i) {
+    const int64_t j = j0 + threadIdx.x + static_cast<int64_t>(i) * kTwoPhaseThreads;
+    if (j < L) {
+      int64_t off;
+      int c;
+      sgn_locate(a, n, g, j, CL, &off, &c);
+      const float sv = sgn_form(a, n, off, c);
+      a.y[off] = from_f32<T>(
+          sgn_out(sv, K, dmean, rstd, to_f32(a.gamma[c]), to_f32(a.beta[c]), a.act));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Test hook: a barrier that can never complete (expects one CTA more than
+// the grid has).  Every CTA gives up after limit_ns and records a timeout.
+// ---------------------------------------------------------------------------
+__global__ void barrier_timeout_probe(Control* ctl, unsigned long long limit_ns) {
+  grid_barrier(ctl, gridDim.x + 1, limit_ns, 99u);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+static int r32(int64_t v) { return static_cast<int>(cdiv(v, 32) * 32); }
+
+size_t group_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int groups) {
+  if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || groups <= 0) return kControlBytes;
+  const int64_t L = (C / groups) * H * W;
+  const int64_t two_phase = N * groups * cdiv(L, kTwoPhaseChunk);
+  const int64_t coop = static_cast<int64_t>(kMaxCoopCtas) * groups;
+  const int64_t slots = two_phase > coop ? two_phase : coop;
+  return kControlBytes + static_cast<size_t>(slots) * sizeof(float4);
+}
+
+template <typename T, typename M, int VE, int NV>
+static void* coop_fn() {
+  return reinterpret_cast<void*>(sgn_nhwc_coop<T, M, VE, NV>);
+}
+
+template <typename T, typename M>
+static void* pick_coop(int ve, int nv) {
+  constexpr int V16 = static_cast<int>(16 / sizeof(T));
+  if (ve == 1) {
+    switch (nv) {
+      case 1: return coop_fn<T, M, 1, 1>();
+      case 2: return coop_fn<T, M, 1, 2>();
+      case 4: return coop_fn<T, M, 1, 4>();
+      case 8: return coop_fn<T, M, 1, 8>();
+    }
+    return nullptr;
+  }
+  switch (nv) {
+    case 1: return coop_fn<T, M, V16, 1>();
+    case 2: return coop_fn<T, M, V16, 2>();
+    case 4: return coop_fn<T, M, V16, 4>();
+    case 8: return coop_fn<T, M, V16, 8>();
+  }
+  return nullptr;
+}
+
+static void* pick_coop_any(DType t, DType m, int ve, int nv) {
+  if (t == DType::F32)
+    return m == DType::F32 ? pick_coop<float, float>(ve, nv) : pick_coop<float, __half>(ve, nv);
+  return m == DType::F32 ? pick_coop<__half, float>(ve, nv) : pick_coop<__half, __half>(ve, nv);
+}
+
+template <typename T, typename M, int VE, int NV>
+static void* resident_fn() {
+  return reinterpret_cast<void*>(sgn_nchw_resident<T, M, VE, NV>);
+}
+
+template <typename T, typename M>
+static void* pick_resident(int ve, int nv) {
+  constexpr int V16 = static_cast<int>(16 / sizeof(T));
+  if (ve == 1) {
+    switch (nv) {
+      case 1: return resident_fn<T, M, 1, 1>();
+      case 2: return resident_fn<T, M, 1, 2>();
+      case 4: return resident_fn<T, M, 1, 4>();
+      case 8: return resident_fn<T, M, 1, 8>();
+    }
+    return nullptr;
+  }
+  switch (nv) {
+    case 1: return resident_fn<T, M, V16, 1>();
+    case 2: return resident_fn<T, M, V16, 2>();
+    case 4: return resident_fn<T, M, V16, 4>();
+    case 8: return resident_fn<T, M, V16, 8>();
+  }
+  return nullptr;
+}
+
+static void* pick_resident_any(DType t, DType m, int ve, int nv) {
+  if (t == DType::F32)
+    return m == DType::F32 ? pick_resident<float, float>(ve, nv)
+                           : pick_resident<float, __half>(ve, nv);
+  return m == DType::F32 ? pick_resident<__half, float>(ve, nv)
+                         : pick_resident<__half, __half>(ve, nv);
+}
+
+static bool resident_cluster_fits(void* fn, int block, int csize) {
+  if (csize > 8 &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(csize);
+  cfg.blockDim = dim3(block);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return clusters > 0;
+}
+
+// Offset (in floats) of the K[groups] tail of route 2's shared memory.
+static size_t coop_k_offset(int PL, int C, int B, int groups) {
+  const size_t phase1 = static_cast<size_t>(PL) + 2ull * PL * C;
+  const size_t phase3 = static_cast<size_t>(B) * groups * 4 + 2ull * groups;
+  return phase1 > phase3 ? phase1 : phase3;
+}
+
+static size_t coop_smem_bytes(int PL, int C, int B, int groups) {
+  return (coop_k_offset(PL, C, B, groups) + groups) * sizeof(float);
+}
+
+GroupPlan two_phase_plan(const SkipGroupCall& c) {
+  const int64_t L = (c.C / c.groups) * c.H * c.W;
+  GroupPlan p = {};
+  p.route = 3;
+  p.ve = 1;
+  p.nv = kTwoPhaseEpt;
+  p.block = kTwoPhaseThreads;
+  p.csize = 1;
+  p.chunks = static_cast<int>(cdiv(L, kTwoPhaseChunk));
+  p.grid = c.N * c.groups * p.chunks;
+  p.smem = 0;
+  return p;
+}
+
+cudaError_t plan_group(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) {
+  *p = GroupPlan{};
+  const int64_t HW = c.H * c.W;
+  const int64_t cpg = c.C / c.groups;
+  const int64_t L = cpg * HW;
+  const int vec_elems = static_cast<int>(16 / dtype_size(c.t));
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+
+  if (!c.channels_last) {
+    // Route 1: the instance must fit in one cluster's registers.
+    const int ve = (vector_ok && HW % vec_elems == 0) ? vec_elems : 1;
+    const int64_t nvec = L / ve;
+    const int64_t insts = c.N * c.groups;
+    int best_nv = -1, best_cta = 0, best_cs = 0;
+    for (int cs = 1; cs <= 16 && best_nv < 0; cs *= 2) {
+      for (int nv : {2, 4, 8}) {
+        const int cta = r32(cdiv(nvec, static_cast<int64_t>(nv) * cs));
+        if (cta > kResidentMaxThreads) continue;
+        best_nv = nv;
+        best_cta = cta < 32 ? 32 : cta;
+        best_cs = cs;
+        break;
+      }
+    }
+    if (best_nv > 0) {
+      // more CTAs per instance when the instances alone under-fill the GPU
+      while (best_cs < 16 && insts * best_cs < 2LL * sms &&
+             r32(cdiv(nvec, static_cast<int64_t>(best_nv) * best_cs * 2)) >= 64) {
+        best_cs *= 2;
+        best_cta = r32(cdiv(nvec, static_cast<int64_t>(best_nv) * best_cs));
+      }
+      void* fn = pick_resident_any(c.t, c.m, ve, best_nv);
+      if (fn && (best_cs == 1 || resident_cluster_fits(fn, best_cta, best_cs)) &&
+          insts * best_cs <= 0x7fffffffLL) {
+        p->route = 1;
+        p->ve = ve;
+        p->nv = best_nv;
+        p->block = best_cta;
+        p->csize = best_cs;
+        p->grid = insts * best_cs;
+        return cudaSuccess;
+      }
+    }
+    *p = two_phase_plan(c);
+    return cudaSuccess;
+  }
+
+  // Route 2: NHWC cooperative.  Every CTA must be resident at once, so the
+  // grid is at most (CTAs per SM) x (SMs); each CTA's pixel slab must fit in
+  // its threads' registers (nv vectors per thread).
+  const int ve = (vector_ok && c.C % vec_elems == 0) ? vec_elems : 1;
+  const int64_t CV = c.C / ve;
+  if (CV <= kCoopMaxThreads && HW <= 0x7fffffffLL) {
+    const int PL = static_cast<int>(kCoopMaxThreads / CV);
+    const int block = static_cast<int>(PL * CV);
+    const size_t smem1 = coop_smem_bytes(PL, static_cast<int>(c.C), 0, c.groups);
+    for (int nv : {1, 2, 4, 8}) {
+      void* fn = pick_coop_any(c.t, c.m, ve, nv);
+      if (!fn || smem1 > kMaxSmemBytes) continue;
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kMaxSmemBytes)) != cudaSuccess) {
+        cudaGetLastError();
+        continue;
+      }
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, block, smem1) != cudaSuccess) {
+        cudaGetLastError();
+        continue;
+      }
+      int64_t cap = static_cast<int64_t>(per_sm) * sms;
+      if (cap > kMaxCoopCtas) cap = kMaxCoopCtas;
+      const int64_t B = cap / c.N;
+      if (B < 1) break;  // more batch items than resident CTAs
+      const int64_t ppc = cdiv(HW, B);
+      if (ppc > static_cast<int64_t>(nv) * PL) continue;  // slab too big for nv
+      const int64_t Bn = cdiv(HW, ppc);  // CTAs actually needed per item
+      const size_t smem = coop_smem_bytes(PL, static_cast<int>(c.C), static_cast<int>(Bn), c.groups);
+      if (smem > kMaxSmemBytes) continue;
+      if (smem > smem1) {
+        int again = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&again, fn, block, smem) != cudaSuccess) {
+          cudaGetLastError();
+          continue;
+        }
+        if (static_cast<int64_t>(again) * sms < Bn * c.N) continue;
+      }
+      p->route = 2;
+      p->ve = ve;
+      p->nv = nv;
+      p->block = block;
+      p->csize = 1;
+      p->ctas_per_item = static_cast<int>(Bn);
+      p->pix_per_cta = static_cast<int>(ppc);
+      p->grid = Bn * c.N;
+      p->smem = smem;
+      return cudaSuccess;
+    }
+  }
+  *p = two_phase_plan(c);
+  return cudaSuccess;
+}
+
+template <typename T, typename M>
+static cudaError_t launch_group_typed(const SkipGroupCall& c, const GroupPlan& p,
+                                      cudaStream_t stream) {
+  SgnArgs<T, M> a;
+  a.x = static_cast<const T*>(c.x);
+  a.skip = static_cast<const T*>(c.skip);
+  a.bias = static_cast<const T*>(c.bias);
+  a.gamma = static_cast<const M*>(c.gamma);
+  a.beta = static_cast<const M*>(c.beta);
+  a.y = static_cast<T*>(c.y);
+  a.s = static_cast<T*>(c.s);
+  a.N = c.N;
+  a.C = static_cast<int>(c.C);
+  a.HW = static_cast<int>(c.H * c.W);
+  a.cpg = static_cast<int>(c.C / c.groups);
+  a.groups = c.groups;
+  a.bcast = c.bcast ? 1 : 0;
+  a.act = c.activation;
+  a.eps = c.eps;
+  a.ctl = static_cast<Control*>(c.workspace);
+  a.part = reinterpret_cast<float4*>(static_cast<char*>(c.workspace) + kControlBytes);
+  a.limit_ns = kWaitLimitNs;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+  cfg.blockDim = dim3(p.block);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+
+  if (p.route == 1) {
+    void* fn = pick_resident<T, M>(p.ve, p.nv);
+    if (!fn) return cudaErrorInvalidConfiguration;
+    if (p.csize > 1) {
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = p.csize;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+    }
+    void* args[] = {&a};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+  }
+  if (p.route == 2) {
+    void* fn = pick_coop<T, M>(p.ve, p.nv);
+    if (!fn) return cudaErrorInvalidConfiguration;
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int B = p.ctas_per_item, ppc = p.pix_per_cta;
+    const int PL = p.block / static_cast<int>(c.C / p.ve);
+    int koff = static_cast<int>(coop_k_offset(PL, static_cast<int>(c.C), B, c.groups));
+    void* args[] = {&a, &B, &ppc, &koff};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+  }
+  // route 3
+  const int chunks = p.chunks;
+  if (c.channels_last) {
+    sgn_partials<T, M, true><<<static_cast<unsigned>(p.grid), p.block, 0, stream>>>(a, chunks);
+    sgn_normalize<T, M, true><<<static_cast<unsigned>(p.grid), p.block, 0, stream>>>(a, chunks);
+  } else {
+    sgn_partials<T, M, false><<<static_cast<unsigned>(p.grid), p.block, 0, stream>>>(a, chunks);
+    sgn_normalize<T, M, false><<<static_cast<unsigned>(p.grid), p.block, 0, stream>>>(a, chunks);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group(const SkipGroupCall& c, const GroupPlan& p, cudaStream_t stream) {
+  if (c.t == DType::F32)
+    return c.m == DType::F32 ? launch_group_typed<float, float>(c, p, stream)
+                             : launch_group_typed<float, __half>(c, p, stream);
+  return c.m == DType::F32 ? launch_group_typed<__half, float>(c, p, stream)
+                           : launch_group_typed<__half, __half>(c, p, stream);
+}
+
+cudaError_t launch_barrier_timeout_probe(void* workspace, unsigned long long limit_ns,
+                                         cudaStream_t stream) {
+  Control* ctl = static_cast<Control*>(workspace);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, barrier_timeout_probe, ctl, limit_ns);
+}
+
+}  // namespace b200norm

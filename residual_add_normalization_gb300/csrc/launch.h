@@ -1,0 +1,110 @@
+// launch.h -- host-side interface between the C ABI (api.cu) and the kernel
+// translation units.  Every function enqueues work on `stream` and returns the
+// CUDA error of the launch (cudaSuccess when nothing needed launching).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace b200norm {
+
+enum class DType { F32 = 0, F16 = 1 };
+
+inline size_t dtype_size(DType t) { return t == DType::F32 ? 4 : 2; }
+
+// Schedule chosen for a row-normalization call (see rows.cuh).
+struct RowPlan {
+  int mode;       // 0: lane groups (tpr <= 32); 1: CTA / cluster per row; 2: walk
+  int ve;         // elements per vector access (16 / sizeof(T)), or 1 (scalar path)
+  int tpr;        // threads per row (mode 0/1), CTA threads (mode 2)
+  int nv;         // vectors held per thread per row
+  int rpg;        // rows per lane group (mode 0)
+  int block;      // threads per CTA
+  int csize;      // CTAs per cluster (mode 1)
+  int64_t grid;   // CTAs
+};
+
+struct SkipRmsCall {
+  const void* x;
+  const void* skip;
+  const void* gamma;
+  const void* bias;
+  void* y;
+  void* s;
+  float* mean;
+  float* inv_std;
+  int64_t rows;
+  int64_t hidden;
+  DType t;
+  float eps;
+};
+
+struct GatedCall {
+  const void* x;
+  const void* gate;
+  const void* scale;
+  void* y;
+  int64_t rows;
+  int64_t C;
+  DType t;
+  float eps;
+};
+
+// Row plans depend only on the shape, element type and pointer alignment.
+RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok);
+
+cudaError_t launch_skip_rms(const SkipRmsCall& c, const RowPlan& p, cudaStream_t stream);
+cudaError_t launch_gated(const GatedCall& c, const RowPlan& p, cudaStream_t stream);
+
+// SkipGroupNorm ------------------------------------------------------------
+struct SkipGroupCall {
+  const void* x;
+  const void* skip;
+  const void* bias;
+  const void* gamma;
+  const void* beta;
+  void* y;
+  void* s;
+  int64_t N, C, H, W;
+  int groups;
+  DType t, m;
+  bool bcast;          // skip holds one value per (n, c)
+  int activation;
+  bool channels_last;
+  float eps;
+  void* workspace;
+  size_t workspace_bytes;
+};
+
+// Route chosen for a SkipGroupNorm call.
+struct GroupPlan {
+  int route;      // 1: NCHW resident (CTA / cluster per group instance)
+                  // 2: NHWC cooperative (grid barrier)
+                  // 3: two-phase partials -> normalize (any shape)
+  int ve;         // elements per vector access, or 1
+  int nv;         // vectors held per thread
+  int block;      // threads per CTA
+  int csize;      // CTAs per cluster (route 1)
+  int64_t grid;   // CTAs
+  int ctas_per_item;   // route 2: CTAs per batch item
+  int pix_per_cta;     // route 2: pixels per CTA
+  int chunks;          // route 3: chunks per group instance
+  size_t smem;         // dynamic shared memory bytes
+};
+
+constexpr size_t kControlBytes = 256;
+constexpr int kTwoPhaseChunk = 4096;   // elements per CTA in route 3
+constexpr int kMaxCoopCtas = 2048;     // upper bound of route-2 grids
+
+size_t group_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int groups);
+cudaError_t plan_group(const SkipGroupCall& c, bool vector_ok, GroupPlan* plan);
+GroupPlan two_phase_plan(const SkipGroupCall& c);
+cudaError_t launch_group(const SkipGroupCall& c, const GroupPlan& p, cudaStream_t stream);
+
+// Test hook: a cooperative grid whose barrier can never complete; the waits
+// give up after `limit_ns` and record a timeout in the workspace.
+cudaError_t launch_barrier_timeout_probe(void* workspace, unsigned long long limit_ns,
+                                         cudaStream_t stream);
+
+}  // namespace b200norm

@@ -1,0 +1,88 @@
+// GatedRMSNorm row kernels (float32 and float16), the row planner, and the
+// SkipSimplifiedLayerNormalization type switch.
+#include "rows_ops.cuh"
+
+#ifndef B200NORM_SHORT_RPG
+#define B200NORM_SHORT_RPG 2   // rows per lane group for spans of <= 16 vectors
+#endif
+#ifndef B200NORM_CTA_NV
+#define B200NORM_CTA_NV 4      // vectors per thread for CTA-per-row schedules
+#endif
+#ifndef B200NORM_PACKED_BLOCK
+#define B200NORM_PACKED_BLOCK 256
+#endif
+
+namespace b200norm {
+
+static int pow2_ceil(int64_t v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+static int round32(int64_t v) { return static_cast<int>(ceil_div(v, 32) * 32); }
+
+RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok) {
+  RowPlan p = {};
+  p.ve = vector_ok ? static_cast<int>(16 / dtype_size(t)) : 1;
+  const int64_t nvec = n / p.ve;
+  p.csize = 1;
+  p.rpg = 1;
+  if (nvec <= 32) {
+    // Short spans: a power-of-two lane group per row, several rows per warp.
+    p.mode = 0;
+    p.tpr = pow2_ceil(nvec);
+    p.nv = 1;
+    p.rpg = p.tpr <= 16 ? B200NORM_SHORT_RPG : 1;
+    p.block = B200NORM_PACKED_BLOCK;
+    p.grid = ceil_div(rows, static_cast<int64_t>(p.block / p.tpr) * p.rpg);
+  } else if (nvec <= 128) {
+    // Warp per row, up to four vectors per lane.
+    p.mode = 0;
+    p.tpr = 32;
+    p.nv = pow2_ceil(ceil_div(nvec, 32));
+    p.block = B200NORM_PACKED_BLOCK;
+    p.grid = ceil_div(rows, p.block / 32);
+  } else {
+    // CTA per row; a cluster per row once one CTA cannot hold it.
+    p.mode = 1;
+    int nv = B200NORM_CTA_NV;
+    int cta = round32(ceil_div(nvec, nv));
+    while (cta > kRowsMaxThreads && nv < 8) {
+      nv *= 2;
+      cta = round32(ceil_div(nvec, nv));
+    }
+    int csize = 1;
+    if (cta > kRowsMaxThreads) {
+      csize = static_cast<int>(ceil_div(nvec, static_cast<int64_t>(nv) * kRowsMaxThreads));
+      cta = round32(ceil_div(nvec, static_cast<int64_t>(nv) * csize));
+    }
+    if (csize > 16) {
+      p.mode = 2;
+      p.tpr = kRowsMaxThreads;
+      p.block = kRowsMaxThreads;
+      p.nv = 1;
+      p.grid = rows;
+      return p;
+    }
+    p.nv = nv;
+    p.csize = csize;
+    p.block = cta;
+    p.tpr = cta * csize;
+    p.grid = rows * csize;
+  }
+  return p;
+}
+
+cudaError_t launch_skip_rms(const SkipRmsCall& c, const RowPlan& p, cudaStream_t st) {
+  return c.t == DType::F32 ? skip_rms_f32(c, p, st) : skip_rms_f16(c, p, st);
+}
+
+cudaError_t launch_gated(const GatedCall& c, const RowPlan& p, cudaStream_t st) {
+  if (c.t == DType::F32) return p.ve == 4 ? gated_go<float, 4>(c, p, st) : gated_go<float, 1>(c, p, st);
+  return p.ve == 8 ? gated_go<__half, 8>(c, p, st) : gated_go<__half, 1>(c, p, st);
+}
+
+}  // namespace b200norm

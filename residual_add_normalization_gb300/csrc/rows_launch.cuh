@@ -1,0 +1,92 @@
+// rows_launch.cuh -- host-side launch of the row kernels for one Op policy.
+#pragma once
+
+#include "launch.h"
+#include "rows.cuh"
+
+namespace b200norm {
+
+template <class Op>
+using RowsKernelFn = void (*)(const typename Op::Args, int, int);
+
+// The (NV, RPG) instantiations every Op provides.
+template <class Op>
+RowsKernelFn<Op> pick_rows_kernel(int nv, int rpg) {
+  if (rpg == 1) {
+    switch (nv) {
+      case 1: return rows_kernel<Op, 1, 1>;
+      case 2: return rows_kernel<Op, 2, 1>;
+      case 4: return rows_kernel<Op, 4, 1>;
+      case 8: return rows_kernel<Op, 8, 1>;
+      default: return nullptr;
+    }
+  }
+  if (nv == 1) {
+    switch (rpg) {
+      case 2: return rows_kernel<Op, 1, 2>;
+      case 4: return rows_kernel<Op, 1, 4>;
+      default: return nullptr;
+    }
+  }
+  return nullptr;
+}
+
+template <class Op>
+cudaError_t launch_rows_op(const typename Op::Args& a, const RowPlan& p, cudaStream_t stream) {
+  const int nvec = static_cast<int>(a.n / p.ve);
+  if (p.mode == 2) {
+    rows_walk_kernel<Op><<<static_cast<unsigned>(p.grid), p.block, 0, stream>>>(a, nvec);
+    return cudaGetLastError();
+  }
+  RowsKernelFn<Op> fn = pick_rows_kernel<Op>(p.nv, p.rpg);
+  if (!fn) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+  cfg.blockDim = dim3(p.block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (p.mode == 1 && p.csize > 1) {
+    if (p.csize > 8) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, fn, a, p.tpr, nvec);
+}
+
+// Can a cluster of `csize` CTAs of `block` threads of this kernel be resident?
+template <class Op>
+bool cluster_fits(int nv, int block, int csize) {
+  RowsKernelFn<Op> fn = pick_rows_kernel<Op>(nv, 1);
+  if (!fn) return false;
+  if (csize > 8 &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(csize);
+  cfg.blockDim = dim3(block);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return clusters > 0;
+}
+
+}  // namespace b200norm

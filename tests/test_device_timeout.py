@@ -1,0 +1,64 @@
+"""The bounded device-side wait: a grid barrier that can never complete gives
+up after its limit, records B200NORM_ERR_DEVICE_TIMEOUT in the workspace, and
+leaves the CUDA context usable.  Nothing here faults or hangs the GPU: the
+probe kernel's only wait is bounded by %globaltimer."""
+import ctypes
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import residual_add_normalization_gb300 as b2
+from residual_add_normalization_gb300 import synthetic
+from helpers import assert_y_close, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+TIMEOUT = 5
+
+
+def test_unsatisfiable_barrier_reports_timeout_and_context_survives():
+    lib = b2.library()
+    ws = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    t0 = time.time()
+    assert lib.b200norm_testing_barrier_timeout(ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                                20_000_000, stream) == 0
+    st = lib.b200norm_workspace_status(ctypes.c_void_p(ws.data_ptr()), stream)
+    elapsed = time.time() - t0
+    assert st == TIMEOUT, lib.b200norm_status_string(st)
+    assert b"gave up" in lib.b200norm_last_error()
+    assert elapsed < 10.0
+    with pytest.raises(b2.B200NormError):
+        b2.workspace_status(ws)
+    # re-initialise, then the same workspace serves a real call
+    b2.workspace_init(ws)
+    b2.workspace_status(ws)
+    d = synthetic.skip_group_inputs((2, 8, 8, 64), np.float16, np.float32, seed=1,
+                                    channels_last=1, skip="nc", bias=True)
+    y, _ = b2.skip_group(to_dev(d["x"]), to_dev(d["skip"]), to_dev(d["gamma"]),
+                         to_dev(d["beta"]), to_dev(d["bias"]), groups=4, activation=1,
+                         workspace=ws)
+    b2.workspace_status(ws)
+    ry, _ = oracle.skip_group(d["x"], d["skip"], d["gamma"], d["beta"], d["bias"], groups=4,
+                              activation=1)
+    assert_y_close(to_host(y), ry)
+
+
+def test_workspace_left_ready_after_many_calls():
+    """The cooperative route's barrier resets itself: many back-to-back calls
+    on one workspace keep working and leave no error."""
+    ws = torch.zeros(b2.workspace_size(2, 320, 64, 64, 32), dtype=torch.uint8, device="cuda")
+    d = synthetic.skip_group_inputs((2, 64, 64, 320), np.float16, np.float32, seed=3,
+                                    channels_last=1, skip="nc", bias=True)
+    args = [to_dev(d[k]) for k in ("x", "skip", "gamma", "beta", "bias")]
+    for _ in range(50):
+        y, _ = b2.skip_group(*args, groups=32, activation=1, workspace=ws)
+    b2.workspace_status(ws)
+    ctl = ws[:16].view(torch.int32).cpu().numpy()
+    assert ctl[0] == 0 and ctl[2] == 0  # count back at zero, no error recorded
+    ry, _ = oracle.skip_group(d["x"], d["skip"], d["gamma"], d["beta"], d["bias"], groups=32,
+                              activation=1)
+    assert_y_close(to_host(y), ry)

@@ -1,0 +1,44 @@
+"""GPU parity at the five reference workloads' full sizes, in the launch
+configuration the benchmark times (the automatic schedule, one call per
+workload on the current stream).  The C oracle computes every output element
+here, so the comparison is element by element, not sampled."""
+import pytest
+import torch
+
+import oracle
+import residual_add_normalization_gb300 as b2
+from residual_add_normalization_gb300 import synthetic
+from helpers import assert_bitexact, assert_y_close, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", synthetic.WORKLOAD_ORDER)
+def test_workload_full_size(name):
+    spec, d = synthetic.workload(name)
+    if spec["op"] == "skip_rms":
+        y, s = b2.skip_rms(to_dev(d["input"]), to_dev(d["skip"]), to_dev(d["gamma"]),
+                           to_dev(d["bias"]), epsilon=spec["epsilon"], want_sum=spec["want_sum"])
+        torch.cuda.synchronize()
+        ry, rs = oracle.skip_rms(d["input"], d["skip"], d["gamma"], d["bias"],
+                                 epsilon=spec["epsilon"])
+        assert_bitexact(to_host(s), rs)
+        assert_y_close(to_host(y), ry)
+    elif spec["op"] == "gated_rms":
+        y = b2.gated_rms(to_dev(d["x"]), to_dev(d["gate"]), to_dev(d["scale"]),
+                         epsilon=spec["epsilon"])
+        torch.cuda.synchronize()
+        ry = oracle.gated_rms(d["x"], d["gate"], d["scale"], epsilon=spec["epsilon"])
+        assert_y_close(to_host(y), ry)
+    else:
+        y, s = b2.skip_group(to_dev(d["x"]), to_dev(d["skip"]), to_dev(d["gamma"]),
+                             to_dev(d["beta"]), to_dev(d["bias"]), groups=spec["groups"],
+                             activation=spec["activation"], epsilon=spec["epsilon"],
+                             channels_last=spec["channels_last"], want_sum=spec["want_sum"])
+        torch.cuda.synchronize()
+        ry, rs = oracle.skip_group(d["x"], d["skip"], d["gamma"], d["beta"], d["bias"],
+                                   groups=spec["groups"], activation=spec["activation"],
+                                   epsilon=spec["epsilon"], channels_last=spec["channels_last"])
+        if spec["want_sum"]:
+            assert_bitexact(to_host(s), rs)
+        assert_y_close(to_host(y), ry)

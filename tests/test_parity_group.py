@@ -1,0 +1,169 @@
+"""GPU parity: SkipGroupNorm kernels against the CPU oracle on the same seeded
+inputs, through the C ABI (via the binding).
+
+Covers the three routes (NCHW resident CTA / cluster per group instance, NHWC
+cooperative grid with a bounded grid barrier, two-phase for anything else),
+both layouts, both T and both M, full / (N, C) / (N, 1, 1, C) skip, bias and S
+on and off, SiLU on and off, vector and scalar paths, and ragged slabs.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import residual_add_normalization_gb300 as b2
+from residual_add_normalization_gb300 import synthetic
+from helpers import assert_bitexact, assert_y_close, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+F32, F16 = 0, 1
+_CODE = {np.float32: F32, np.float16: F16}
+
+
+@pytest.fixture(autouse=True)
+def _reset_force():
+    yield
+    b2.library().b200norm_testing_force(0, 0)
+
+
+def plan(shape, groups, dtype, mdtype, cl):
+    if cl:
+        N, H, W, C = shape
+    else:
+        N, C, H, W = shape
+    out = (ctypes.c_int64 * 8)()
+    st = b2.library().b200norm_testing_plan_group(N, C, H, W, groups, _CODE[dtype], _CODE[mdtype],
+                                                  cl, 1, out)
+    assert st == 0
+    return dict(zip(("route", "ve", "nv", "block", "csize", "grid", "B", "ppc"), out))
+
+
+def run(d, groups, act, cl, eps=1e-5, want_sum=True):
+    y, s = b2.skip_group(to_dev(d["x"]), to_dev(d["skip"]), to_dev(d["gamma"]),
+                         to_dev(d["beta"]), to_dev(d["bias"]), groups=groups, activation=act,
+                         epsilon=eps, channels_last=cl, want_sum=want_sum)
+    torch.cuda.synchronize()
+    return to_host(y), to_host(s)
+
+
+def check(d, groups, act, cl, eps=1e-5, want_sum=True):
+    y, s = run(d, groups, act, cl, eps, want_sum)
+    ry, rs = oracle.skip_group(d["x"], d["skip"], d["gamma"], d["beta"], d["bias"],
+                               groups=groups, activation=act, epsilon=eps, channels_last=cl)
+    if want_sum:
+        assert_bitexact(s, rs)
+    else:
+        assert s is None
+    assert_y_close(y, ry)
+
+
+# (logical N, C, H, W, groups)
+NCHW_CASES = [
+    (2, 8, 3, 2, 2),        # usage-example sizes, scalar path (H*W = 6)
+    (2, 12, 5, 7, 4),       # odd H*W: scalar path
+    (3, 64, 8, 8, 8),       # small instances
+    (2, 1280, 16, 16, 32),  # 10,240-element instances (the wide-group workload's)
+    (1, 320, 64, 64, 32),   # 40,960-element instances: clusters
+    (1, 64, 128, 128, 1),   # one 1M-element instance: two-phase
+    (4, 6, 1, 1, 6),        # one element per group
+]
+
+
+@pytest.mark.parametrize("dtype,mdtype", [(np.float32, np.float16), (np.float16, np.float32),
+                                          (np.float16, np.float16), (np.float32, np.float32)])
+@pytest.mark.parametrize("case", NCHW_CASES)
+def test_nchw_matches_oracle(dtype, mdtype, case):
+    N, C, H, W, G = case
+    for skip, bias, act, want_sum in (("full", False, 0, False), ("nc", True, 1, True)):
+        d = synthetic.skip_group_inputs((N, C, H, W), dtype, mdtype, seed=N * C + H,
+                                        channels_last=0, skip=skip, bias=bias, x_std=2.0)
+        check(d, G, act, 0, want_sum=want_sum)
+
+
+# (logical N, H, W, C, groups)
+NHWC_CASES = [
+    (2, 3, 2, 8, 2),        # the usage example's shape
+    (2, 64, 64, 320, 32),   # the NHWC workload's shape
+    (2, 8, 8, 64, 4),
+    (3, 5, 7, 12, 3),       # C % 8 != 0: scalar path
+    (1, 33, 17, 40, 8),     # ragged last slab
+    (2, 16, 16, 4104, 8),   # C / 8 = 513 vectors per pixel: two-phase
+    (600, 2, 2, 16, 4),     # more batch items than resident CTAs: two-phase
+    (4, 1, 1, 6, 6),
+]
+
+
+@pytest.mark.parametrize("dtype,mdtype", [(np.float16, np.float32), (np.float32, np.float16),
+                                          (np.float16, np.float16), (np.float32, np.float32)])
+@pytest.mark.parametrize("case", NHWC_CASES)
+def test_nhwc_matches_oracle(dtype, mdtype, case):
+    N, H, W, C, G = case
+    for skip, bias, act, want_sum in (("nc", True, 1, True), ("full", False, 0, False),
+                                      ("n11c", True, 0, True)):
+        d = synthetic.skip_group_inputs((N, H, W, C), dtype, mdtype, seed=N + H * W + C,
+                                        channels_last=1, skip=skip, bias=bias)
+        check(d, G, act, 1, want_sum=want_sum)
+
+
+@pytest.mark.parametrize("cl", [0, 1])
+@pytest.mark.parametrize("dtype", [np.float32, np.float16])
+def test_forced_two_phase(cl, dtype):
+    assert b2.library().b200norm_testing_force(0, 3) == 0
+    shape = (2, 16, 16, 64) if cl else (2, 64, 16, 16)
+    d = synthetic.skip_group_inputs(shape, dtype, np.float32, seed=7, channels_last=cl,
+                                    skip="nc", bias=True)
+    check(d, 8, 1, cl)
+
+
+def test_route_coverage():
+    routes = set()
+    for N, C, H, W, G in NCHW_CASES:
+        p = plan((N, C, H, W), G, np.float16, np.float32, 0)
+        routes.add((p["route"], p["csize"] > 1))
+    for N, H, W, C, G in NHWC_CASES:
+        routes.add((plan((N, H, W, C), G, np.float16, np.float32, 1)["route"], False))
+    assert {r for r, _ in routes} == {1, 2, 3}
+    assert (1, True) in routes, "no cluster-per-instance case"
+
+
+def test_n11c_at_hw1_equals_nc_route():
+    d = synthetic.skip_group_inputs((3, 1, 1, 16), np.float16, np.float32, seed=4,
+                                    channels_last=1, skip="n11c", bias=True)
+    y1, s1 = run(d, 4, 1, 1)
+    d2 = dict(d, skip=d["skip"].reshape(3, 16))
+    y2, s2 = run(d2, 4, 1, 1)
+    assert_bitexact(y1, y2, "Y")
+    assert_bitexact(s1, s2)
+
+
+def test_y_independent_of_s_request():
+    d = synthetic.skip_group_inputs((2, 16, 16, 64), np.float16, np.float32, seed=9,
+                                    channels_last=1, skip="full", bias=True)
+    y1, _ = run(d, 8, 1, 1, want_sum=True)
+    y2, _ = run(d, 8, 1, 1, want_sum=False)
+    assert_bitexact(y1, y2, "Y")
+
+
+def test_large_mean_small_variance():
+    """Groups whose mean is far from zero against their spread: carrying the
+    mean as an exact data value plus a small offset keeps float32 Y inside
+    1e-5."""
+    for cl, shape in ((0, (2, 64, 16, 16)), (1, (2, 16, 16, 64))):
+        d = synthetic.skip_group_inputs(shape, np.float32, np.float32, seed=12,
+                                        channels_last=cl, skip="full", bias=False,
+                                        x_mean=1000.0, x_std=0.5)
+        check(d, 8, 0, cl)
+        assert b2.library().b200norm_testing_force(0, 3) == 0
+        check(d, 8, 0, cl)
+        assert b2.library().b200norm_testing_force(0, 0) == 0
+
+
+def test_empty_batch():
+    x = torch.empty((0, 4, 4, 8), dtype=torch.float16, device="cuda")
+    g = torch.ones(8, dtype=torch.float32, device="cuda")
+    y, s = b2.skip_group(x, torch.empty((0, 8), dtype=torch.float16, device="cuda"), g, g,
+                         groups=2, activation=0)
+    assert y.shape == x.shape
