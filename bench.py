@@ -1,0 +1,450 @@
+"""Benchmark: effective HBM GB/s of the fused residual-add + normalization path.
+
+One step = one call of each operator on its large workload, i.e. one pass of
+the whole hot path:
+  SkipSimplifiedLayerNormalization fp16 (8, 2048, 4096), bias, S
+  GatedRMSNorm fp16 (4, 4096, 8192), C = 128
+  SkipGroupNorm NHWC fp16 (2, 64, 64, 320), (N, C) skip, bias, S, SiLU
+  SkipGroupNorm NCHW fp32 (16, 1280, 16, 16), full skip, fp16 gamma/beta
+value = algorithmic bytes (every input element read once, every output
+written once) / device time, summed over the step.  A step moves 1.42 GB, far
+more than the 129 MB L2, so every operator starts with its inputs evicted by
+the other operators' traffic.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
+operators have no cross-device step); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from residual_add_normalization_gb300 import synthetic  # noqa: E402
+
+METRIC = ("effective HBM GB/s and % of GB300 peak per op; rows/s (1 GPU, device-timed)")
+STEP_WORKLOADS = ["ssln_fp16_8x2048x4096", "gated_fp16_4x4096x8192_c128",
+                  "sgn_nhwc_fp16_2x64x64x320", "sgn_nchw_fp32_16x1280x16x16"]
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by
+# the digest of the kernel sources it was taken on (None: not captured for
+# the current sources).
+NCU_TRAFFIC = {}
+
+
+def peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [f.strip() for f in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        note = "sampled during the timed region"
+        if not inside and self.samples:
+            # timed region shorter than the sampling period: nearest samples
+            inside = [min(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))[1]]
+            note = "timed region shorter than the sampling period; nearest sample"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no samples"}
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in inside if num(s[0]) is not None]
+        mx = [num(s[1]) for s in inside if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4)
+                          if len(s) > 4 + i and s[4 + i].lower().startswith("active")})
+        pw = [num(s[2]) for s in inside if num(s[2]) is not None]
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max(pw) if pw else None, "samples": len(inside), "note": note}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def make_calls(torch, b2, dev):
+    """Device inputs, preallocated outputs and one closure per workload."""
+    calls = []
+    for name in STEP_WORKLOADS:
+        spec, d = synthetic.workload(name)
+        t = {k: (None if v is None else torch.from_numpy(v).to(dev)) for k, v in d.items()}
+        if spec["op"] == "skip_rms":
+            y, s = torch.empty_like(t["input"]), torch.empty_like(t["input"])
+            def fn(t=t, y=y, s=s, spec=spec):
+                b2.skip_rms(t["input"], t["skip"], t["gamma"], t["bias"],
+                            epsilon=spec["epsilon"], output=y, sum_out=s)
+            outs = [y, s]
+        elif spec["op"] == "gated_rms":
+            y = torch.empty_like(t["x"])
+            def fn(t=t, y=y, spec=spec):
+                b2.gated_rms(t["x"], t["gate"], t["scale"], epsilon=spec["epsilon"], y=y)
+            outs = [y]
+        else:
+            y = torch.empty_like(t["x"])
+            s = torch.empty_like(t["x"]) if spec["want_sum"] else None
+            def fn(t=t, y=y, s=s, spec=spec):
+                b2.skip_group(t["x"], t["skip"], t["gamma"], t["beta"], t["bias"],
+                              groups=spec["groups"], activation=spec["activation"],
+                              epsilon=spec["epsilon"], channels_last=spec["channels_last"],
+                              y=y, s=s)
+            outs = [y] + ([s] if s is not None else [])
+        calls.append(dict(name=name, spec=spec, fn=fn, inputs=t, outs=outs,
+                          host=d, bytes=synthetic.algorithmic_bytes(name),
+                          units=synthetic.units(name)))
+    return calls
+
+
+def launches_per_call(b2, spec):
+    import ctypes
+    if spec["op"] != "skip_group":
+        return 1
+    shape = spec["shape"]
+    N, C, H, W = ((shape[0], shape[3], shape[1], shape[2]) if spec["channels_last"]
+                  else shape)
+    code = {np.dtype(np.float32): 0, np.dtype(np.float16): 1}
+    out = (ctypes.c_int64 * 8)()
+    b2.library().b200norm_testing_plan_group(N, C, H, W, spec["groups"],
+                                             code[np.dtype(spec["dtype"])],
+                                             code[np.dtype(spec["mdtype"])],
+                                             spec["channels_last"], 1, out)
+    return 2 if out[0] == 3 else 1
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    import residual_add_normalization_gb300 as b2
+    from residual_add_normalization_gb300 import buildlib
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    b2.library()  # raises if the CUDA library is missing: no fallback
+    calls = make_calls(torch, b2, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for c in calls:
+            c["fn"]()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # --- device-timed region: K steps, an event pair around every call -----
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+          for _ in range(args.steps)]
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(args.steps):
+        for i, c in enumerate(calls):
+            ev[k][i].record(stream)
+            c["fn"]()
+        ev[k][-1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    time.sleep(0.1)
+    clocks.stop()
+    total_ms = start.elapsed_time(end)
+    per_call_ms = np.zeros(len(calls))
+    for k in range(args.steps):
+        for i in range(len(calls)):
+            per_call_ms[i] += ev[k][i].elapsed_time(ev[k][i + 1])
+    per_call_ms /= args.steps
+    if dist:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # --- end to end through the public API with host buffers ---------------
+    e2e_steps = 0 if args.no_e2e else min(args.steps, 20)
+    pinned_in = [{k: (None if v is None or not e2e_steps else torch.from_numpy(v).pin_memory())
+                  for k, v in c["host"].items()} for c in calls]
+    pinned_out = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in c["outs"]]
+                  if e2e_steps else [] for c in calls]
+    h2d = sum(v.numel() * v.element_size() for d in pinned_in for v in d.values()
+              if v is not None)
+    d2h = sum(o.numel() * o.element_size() for c in calls for o in c["outs"])
+
+    def e2e_step():
+        for c, pin, pout in zip(calls, pinned_in, pinned_out):
+            for k, v in pin.items():
+                if v is not None:
+                    c["inputs"][k].copy_(v, non_blocking=True)
+            c["fn"]()
+            for o, p in zip(c["outs"], pout):
+                p.copy_(o, non_blocking=True)
+
+    e2e_ms = float("nan")
+    if e2e_steps:
+        e2e_step()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return None
+
+    step_bytes = sum(c["bytes"] for c in calls)
+    ms_per_step = total_ms / args.steps
+    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    peak, peak_src = peak_hbm()
+    per_op = {}
+    for c, ms in zip(calls, per_call_ms):
+        gbs = c["bytes"] / (ms * 1e-3) / 1e9
+        per_op[c["name"]] = {
+            "us_per_call": round(ms * 1e3, 3), "GB_s": round(gbs, 1),
+            "frac_of_measured_peak": round(gbs / peak, 4),
+            "frac_of_8TBs_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+            "units_per_s": round(c["units"] / (ms * 1e-3), 1),
+            "units": {"skip_rms": "rows", "gated_rms": "C-spans",
+                      "skip_group": "group instances"}[c["spec"]["op"]],
+            "algorithmic_bytes": c["bytes"]}
+    dom = int(np.argmax(per_call_ms))
+    dom_c = calls[dom]
+    achieved = dom_c["bytes"] / (per_call_ms[dom] * 1e-3) / 1e9
+    digest = buildlib.source_digest()
+    traffic = NCU_TRAFFIC.get((dom_c["name"], digest))
+    launches = sum(launches_per_call(b2, c["spec"]) for c in calls) * args.steps
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": " + ".join(STEP_WORKLOADS),
+            "bytes_per_step": step_bytes,
+            "storage_types": "f16 / f32 tensors (fp32 arithmetic, one rounding at each store)",
+            "l2": "inputs larger than L2: a step moves 1.42 GB against a 129 MB L2",
+            "parallelism": f"replicas x{world}",
+        },
+        "per_op": per_op,
+        "roofline": {"bound": "hbm", "kernel": dom_c["name"], "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": peak_src, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dom_c["bytes"]},
+        "e2e": ({"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                 "steps": e2e_steps, "ms_per_step": round(e2e_ms, 3)} if e2e_steps else None),
+        "gpu_launches": launches,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        "source_digest": digest,
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (the baseline and the reference arm)
+# ---------------------------------------------------------------------------
+_WORKLOAD_CACHE = {}
+
+
+def _workload(name):
+    if name not in _WORKLOAD_CACHE:
+        _WORKLOAD_CACHE[name] = synthetic.workload(name)
+    return _WORKLOAD_CACHE[name]
+
+
+def oracle_sample(fraction):
+    """Run the oracle on ``fraction`` of every step workload (leading rows /
+    spans / batch items) and return (algorithmic bytes covered, seconds)."""
+    import oracle
+    total_bytes, total_s = 0.0, 0.0
+    for name in STEP_WORKLOADS:
+        spec, d = _workload(name)
+        shape = spec["shape"]
+        lead = max(1, int(round(shape[0] * fraction)))
+        if spec["op"] == "skip_rms":
+            rows = max(1, int(round(np.prod(shape[:-1]) * fraction)))
+            x = d["input"].reshape(-1, shape[-1])[:rows]
+            sk = d["skip"].reshape(-1, shape[-1])[:rows]
+            t0 = time.perf_counter()
+            oracle.skip_rms(x, sk, d["gamma"], d["bias"], epsilon=spec["epsilon"])
+            total_s += time.perf_counter() - t0
+            total_bytes += synthetic.algorithmic_bytes(name) * rows / np.prod(shape[:-1])
+        elif spec["op"] == "gated_rms":
+            spans = max(1, int(round(np.prod(shape) // spec["C"] * fraction)))
+            x = d["x"].reshape(-1, spec["C"])[:spans]
+            g = d["gate"].reshape(-1, spec["C"])[:spans]
+            t0 = time.perf_counter()
+            oracle.gated_rms(x, g, d["scale"], epsilon=spec["epsilon"])
+            total_s += time.perf_counter() - t0
+            total_bytes += synthetic.algorithmic_bytes(name) * spans / (np.prod(shape) // spec["C"])
+        else:
+            x = d["x"][:lead]
+            sk = d["skip"][:lead]
+            t0 = time.perf_counter()
+            oracle.skip_group(x, sk, d["gamma"], d["beta"], d["bias"], groups=spec["groups"],
+                              activation=spec["activation"], epsilon=spec["epsilon"],
+                              channels_last=spec["channels_last"], want_sum=spec["want_sum"])
+            total_s += time.perf_counter() - t0
+            total_bytes += synthetic.algorithmic_bytes(name) * lead / shape[0]
+    return total_bytes, total_s
+
+
+def cpu_baseline(budget_s=15.0):
+    b, s = oracle_sample(1 / 64)
+    frac = min(1.0, (1 / 64) * budget_s / max(s, 1e-3))
+    b, s = oracle_sample(frac)
+    return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"leading {frac:.4f} of the rows / C-spans / batch items of each step "
+                      f"workload, single-threaded C oracle ({s:.1f} s)"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is a bounded slice of the
+    step workloads, sized so the whole run takes about a minute."""
+    import oracle
+    oracle.build()
+    b, s = oracle_sample(1 / 256)
+    per_step = 60.0 / max(1, args.steps + args.warmup)
+    frac = min(1.0, (1 / 256) * per_step / max(s, 1e-4))
+    for _ in range(args.warmup):
+        oracle_sample(frac)
+    tb, ts = 0.0, 0.0
+    for _ in range(args.steps):
+        bb, ss = oracle_sample(frac)
+        tb += bb
+        ts += ss
+    value = tb / ts / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ts / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": " + ".join(STEP_WORKLOADS),
+                       "sample_fraction_per_step": frac},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"leading {frac:.6f} of each step workload per step"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer end-to-end leg (for profiler runs)")
+    ap.add_argument("--only", choices=STEP_WORKLOADS,
+                    help="run a single workload (for profiler runs; not a bench line)")
+    args = ap.parse_args()
+    if args.only:
+        STEP_WORKLOADS[:] = [args.only]
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    line = run_ours(args, rank, world, dist)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -55,7 +55,6 @@ constexpr int kResidentMaxThreads = 512;
 constexpr int kCoopMaxThreads = 512;
 constexpr int kTwoPhaseThreads = 256;
 constexpr int kTwoPhaseEpt = kTwoPhaseChunk / kTwoPhaseThreads;
-constexpr size_t kMaxSmemBytes = 227 * 1024;
 
 // S element at type T from binary32 x and skip, plus bias when present.
 template <typename T>
@@ -664,9 +663,20 @@ cudaError_t plan_group(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) {
     const size_t smem1 = coop_smem_bytes(PL, static_cast<int>(c.C), 0, c.groups);
     for (int nv : {1, 2, 4, 8}) {
       void* fn = pick_coop_any(c.t, c.m, ve, nv);
-      if (!fn || smem1 > kMaxSmemBytes) continue;
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kMaxSmemBytes)) != cudaSuccess) {
+      if (!fn) continue;
+      // dynamic + static shared memory must fit the per-block opt-in limit
+      cudaFuncAttributes fa;
+      int optin = 0;
+      if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess ||
+          cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+              cudaSuccess) {
+        cudaGetLastError();
+        continue;
+      }
+      const size_t smem_cap = static_cast<size_t>(optin) - fa.sharedSizeBytes;
+      if (smem1 > smem_cap ||
+          cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem_cap)) != cudaSuccess) {
         cudaGetLastError();
         continue;
       }
@@ -683,7 +693,7 @@ cudaError_t plan_group(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) {
       if (ppc > static_cast<int64_t>(nv) * PL) continue;  // slab too big for nv
       const int64_t Bn = cdiv(HW, ppc);  // CTAs actually needed per item
       const size_t smem = coop_smem_bytes(PL, static_cast<int>(c.C), static_cast<int>(Bn), c.groups);
-      if (smem > kMaxSmemBytes) continue;
+      if (smem > smem_cap) continue;
       if (smem > smem1) {
         int again = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&again, fn, block, smem) != cudaSuccess) {

@@ -21,7 +21,7 @@ TIMEOUT = 5
 
 def test_unsatisfiable_barrier_reports_timeout_and_context_survives():
     lib = b2.library()
-    ws = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(b2.workspace_size(2, 64, 8, 8, 4), dtype=torch.uint8, device="cuda")
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     t0 = time.time()
     assert lib.b200norm_testing_barrier_timeout(ctypes.c_void_p(ws.data_ptr()), ws.numel(),
