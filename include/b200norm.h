@@ -189,6 +189,38 @@ B200NORM_API b200norm_status b200norm_skip_group(
     int64_t W, b200norm_dtype T, b200norm_dtype M, int groups, float epsilon, int activation,
     int channels_last, void* workspace, size_t workspace_bytes, b200norm_stream_t stream);
 
+/*
+ * SkipGroupNorm without a workspace, for callers that cannot allocate device
+ * memory: for example a plugin whose host passes it only its input and output
+ * buffers and provides no allocator, or a service that reserved its device
+ * memory up front and must not allocate (and possibly fail or synchronise)
+ * while serving a request.  The operator pages have no counterpart of this
+ * entry point; it exists only because of that constraint.
+ *
+ * Arguments and results are those of b200norm_skip_group without
+ * `workspace` / `workspace_bytes`.  Instead the library uses a fixed scratch
+ * array of 256 + 2 MiB bytes in device memory, which every GPU that loads
+ * the library holds until the process exits.  That covers up to 64 groups
+ * on every route; a shape that needs more returns B200NORM_ERR_UNSUPPORTED
+ * (see b200norm_last_error) and enqueues nothing -- use b200norm_skip_group
+ * with a workspace for it.  No call allocates or frees memory.
+ *
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress) with that device current.  Make that first call
+ *     before any stream capture begins.
+ *   - Each call clears the array's 256-byte control block on `stream` before
+ *     its kernels; the rest keeps the previous call's contents and is always
+ *     written before it is read.
+ *   - All calls on a device share the one array: calls whose work overlaps on
+ *     the GPU (different streams without ordering between them) race and give
+ *     undefined results.  Order them, e.g. issue them on one stream.
+ */
+B200NORM_API b200norm_status b200norm_skip_group_noalloc(
+    const void* x, const void* skip, int skip_rank, const int64_t* skip_dims, const void* bias,
+    const void* gamma, const void* beta, void* y, void* s, int64_t N, int64_t C, int64_t H,
+    int64_t W, b200norm_dtype T, b200norm_dtype M, int groups, float epsilon, int activation,
+    int channels_last, b200norm_stream_t stream);
+
 /* Zero-fill a SkipGroupNorm workspace (cudaMemsetAsync on `stream`). */
 B200NORM_API b200norm_status b200norm_workspace_init(void* workspace, size_t workspace_bytes,
                                                      b200norm_stream_t stream);

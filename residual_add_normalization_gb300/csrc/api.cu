@@ -149,6 +149,8 @@ int classify_skip(int rank, const int64_t* d, int64_t N, int64_t C, int64_t H, i
 
 }  // namespace
 
+void b200norm::set_error_message(const char* msg) { g_error = msg; }
+
 extern "C" {
 
 int b200norm_version(void) { return 1; }

@@ -102,6 +102,9 @@ cudaError_t plan_group(const SkipGroupCall& c, bool vector_ok, GroupPlan* plan);
 GroupPlan two_phase_plan(const SkipGroupCall& c);
 cudaError_t launch_group(const SkipGroupCall& c, const GroupPlan& p, cudaStream_t stream);
 
+// Set the thread-local message that b200norm_last_error() returns.
+void set_error_message(const char* msg);
+
 // Test hook: a cooperative grid whose barrier can never complete; the waits
 // give up after `limit_ns` and record a timeout in the workspace.
 cudaError_t launch_barrier_timeout_probe(void* workspace, unsigned long long limit_ns,
