@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace b200norm {
 
 // ---------------------------------------------------------------------------
@@ -63,6 +65,57 @@ __device__ __forceinline__ void st_stream(T* p, const Pack<T, N>& v) {
   R r;
   memcpy(&r, &v, sizeof(R));
   __stcs(reinterpret_cast<R*>(p), r);
+}
+
+// Widen a pack to binary32 (pairs of halves convert with one instruction).
+template <typename T, int N>
+__device__ __forceinline__ void unpack(const Pack<T, N>& p, float (&f)[N]) {
+  if constexpr (std::is_same<T, __half>::value && N % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      const float2 t = __half22float2(reinterpret_cast<const __half2*>(p.v)[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) f[i] = to_f32(p.v[i]);
+  }
+}
+
+// Narrow binary32 values to a pack, each rounded to nearest-even.
+template <typename T, int N>
+__device__ __forceinline__ Pack<T, N> pack_from(const float (&f)[N]) {
+  Pack<T, N> p;
+  if constexpr (std::is_same<T, __half>::value && N % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i)
+      reinterpret_cast<__half2*>(p.v)[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) p.v[i] = from_f32<T>(f[i]);
+  }
+  return p;
+}
+
+// Element pair (2i, 2i+1) of a pack as binary32, and the reverse (each value
+// rounded to nearest-even).  For halves one instruction converts both.
+template <typename T, int N>
+__device__ __forceinline__ float2 get2(const Pack<T, N>& p, int i) {
+  if constexpr (std::is_same<T, __half>::value)
+    return __half22float2(reinterpret_cast<const __half2*>(p.v)[i]);
+  else
+    return make_float2(to_f32(p.v[2 * i]), to_f32(p.v[2 * i + 1]));
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void set2(Pack<T, N>& p, int i, float a, float b) {
+  if constexpr (std::is_same<T, __half>::value)
+    reinterpret_cast<__half2*>(p.v)[i] = __floats2half2_rn(a, b);
+  else {
+    p.v[2 * i] = from_f32<T>(a);
+    p.v[2 * i + 1] = from_f32<T>(b);
+  }
 }
 
 // The residual sum at type T: binary32 (x + skip), then + bias when present,

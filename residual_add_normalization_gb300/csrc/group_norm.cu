@@ -51,7 +51,6 @@ struct SgnArgs {
 };
 
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
-constexpr int kResidentMaxThreads = 512;
 constexpr int kCoopMaxThreads = 512;
 constexpr int kTwoPhaseThreads = 256;
 constexpr int kTwoPhaseEpt = kTwoPhaseChunk / kTwoPhaseThreads;
@@ -81,15 +80,47 @@ __device__ __forceinline__ float sgn_shift(const SgnArgs<T, M>& a, int64_t n, in
   return to_f32(sgn_sum<T>(to_f32(a.x[off]), sk, a.bias, c));
 }
 
+// Division by an invariant divisor as a multiply and a shift (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994):
+// for 0 <= n < 2^31, n / d = (umulhi(n, m) + n) >> l with l = ceil(log2 d) and
+// m = floor(2^32 * (2^l - d) / d) + 1.
+struct FastDiv {
+  unsigned m, l;
+};
+
+inline FastDiv make_fastdiv(unsigned d) {
+  unsigned l = 0;
+  while ((1ull << l) < d) ++l;
+  FastDiv f;
+  f.m = static_cast<unsigned>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+  f.l = l;
+  return f;
+}
+
+__device__ __forceinline__ unsigned fdiv(unsigned n, FastDiv f) {
+  return (__umulhi(n, f.m) + n) >> f.l;
+}
+
 // ---------------------------------------------------------------------------
-// Route 1: NCHW, one CTA or cluster per group instance
+// Route 1: NCHW, one CTA or cluster per group instance, S staged in shared
+// memory
 // ---------------------------------------------------------------------------
-// VE elements per access; requires H*W % VE == 0 so an access never straddles
-// two channels.  Thread t of cluster rank r holds vectors
-// t + r*blockDim + k*(blockDim*csize), k < NV.
-template <typename T, typename M, int VE, int NV>
-__global__ void __launch_bounds__(kResidentMaxThreads)
-sgn_nchw_resident(const SgnArgs<T, M> a) {
+// A group instance (n, g) is the contiguous run of L = cpg * H * W elements at
+// (n*C + g*cpg) * H*W.  CTA rank r of the instance's cluster takes vectors
+// [r * span, (r + 1) * span) of it: it loads X (+ skip), forms S, keeps S in
+// shared memory (span vectors of dynamic shared memory), and takes exact
+// two-pass statistics from there; cluster partial sums meet through DSMEM.
+// VE > 1 needs H*W % VE == 0 so that a vector never straddles two channels;
+// vpc = H*W / VE vectors per channel.
+constexpr int kNchwThreads = 256;
+constexpr int kNchwUnroll = 4;
+
+template <typename T, typename M, int VE>
+__global__ void __launch_bounds__(kNchwThreads, 4)
+sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
+  using P = Pack<T, VE>;
+  extern __shared__ float4 smem4[];
+  P* sb = reinterpret_cast<P*>(smem4);
   __shared__ float red[33];
   __shared__ float slot_sum, slot_m2;
   const unsigned csize = cluster_size();
@@ -98,67 +129,65 @@ sgn_nchw_resident(const SgnArgs<T, M> a) {
   const int64_t n = inst / a.groups;
   const int g = static_cast<int>(inst % a.groups);
   const int L = a.cpg * a.HW;
-  const int nvec = L / VE;
-  const int tpr = blockDim.x * csize;
-  const int first = threadIdx.x + static_cast<int>(rank) * blockDim.x;
-  const int64_t base = (n * a.C + static_cast<int64_t>(g) * a.cpg) * a.HW;
+  const int v0 = static_cast<int>(rank) * span;
+  const int cnt = min(span, L / VE - v0);  // may be <= 0 for trailing ranks
+  const int64_t base = (n * a.C + static_cast<int64_t>(g) * a.cpg) * a.HW + static_cast<int64_t>(v0) * VE;
+  const int cbase = g * a.cpg;
 
-  Pack<T, VE> xv[NV], kv[NV], sv[NV];
-#pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int v = first + k * tpr;
-    if (v < nvec) {
-      xv[k] = ld_stream<T, VE>(a.x + base + static_cast<int64_t>(v) * VE);
-      if (!a.bcast) kv[k] = ld_stream<T, VE>(a.skip + base + static_cast<int64_t>(v) * VE);
-    }
-  }
   const float K = sgn_shift(a, n, g, false);
   float sum = 0.0f;
+  for (int i0 = threadIdx.x; i0 < cnt; i0 += kNchwThreads * kNchwUnroll) {
+    P xv[kNchwUnroll], kv[kNchwUnroll];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int v = first + k * tpr;
-    if (v < nvec) {
-      const int c = g * a.cpg + (v * VE) / a.HW;
-      const float skb = a.bcast ? to_f32(a.skip[n * a.C + c]) : 0.0f;
-#pragma unroll
-      for (int e = 0; e < VE; ++e) {
-        const float sk = a.bcast ? skb : to_f32(kv[k].v[e]);
-        sv[k].v[e] = sgn_sum<T>(to_f32(xv[k].v[e]), sk, a.bias, c);
-        sum += to_f32(sv[k].v[e]) - K;
+    for (int u = 0; u < kNchwUnroll; ++u) {
+      const int i = i0 + u * kNchwThreads;
+      if (i < cnt) {
+        xv[u] = ld_stream<T, VE>(a.x + base + static_cast<int64_t>(i) * VE);
+        if (!a.bcast) kv[u] = ld_stream<T, VE>(a.skip + base + static_cast<int64_t>(i) * VE);
       }
-      if (a.s) st_stream<T, VE>(a.s + base + static_cast<int64_t>(v) * VE, sv[k]);
+    }
+#pragma unroll
+    for (int u = 0; u < kNchwUnroll; ++u) {
+      const int i = i0 + u * kNchwThreads;
+      if (i < cnt) {
+        const int c = cbase + static_cast<int>(fdiv(static_cast<unsigned>(v0 + i), vpc));
+        const float skb = a.bcast ? to_f32(a.skip[n * a.C + c]) : 0.0f;
+        P sv;
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          const float sk = a.bcast ? skb : to_f32(kv[u].v[e]);
+          sv.v[e] = sgn_sum<T>(to_f32(xv[u].v[e]), sk, a.bias, c);
+          sum += to_f32(sv.v[e]) - K;
+        }
+        sb[i] = sv;
+        if (a.s) st_stream<T, VE>(a.s + base + static_cast<int64_t>(i) * VE, sv);
+      }
     }
   }
   float tot = cta_sum(sum, red);
   if (csize > 1) tot = cluster_sum(tot, &slot_sum, csize);
   const float dmean = tot / static_cast<float>(L);  // mean = K + dmean
   float m2 = 0.0f;
+  for (int i = threadIdx.x; i < cnt; i += kNchwThreads) {
+    const P sv = sb[i];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int v = first + k * tpr;
-    if (v < nvec) {
-#pragma unroll
-      for (int e = 0; e < VE; ++e) {
-        const float d = (to_f32(sv[k].v[e]) - K) - dmean;
-        m2 = fmaf(d, d, m2);
-      }
+    for (int e = 0; e < VE; ++e) {
+      const float d = (to_f32(sv.v[e]) - K) - dmean;
+      m2 = fmaf(d, d, m2);
     }
   }
   tot = cta_sum(m2, red);
   if (csize > 1) tot = cluster_sum(tot, &slot_m2, csize);
   const float rstd = 1.0f / sqrtf(tot / static_cast<float>(L) + a.eps);
+  for (int i = threadIdx.x; i < cnt; i += kNchwThreads) {
+    const int c = cbase + static_cast<int>(fdiv(static_cast<unsigned>(v0 + i), vpc));
+    const float ga = to_f32(a.gamma[c]), be = to_f32(a.beta[c]);
+    const P sv = sb[i];
+    P out;
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int v = first + k * tpr;
-    if (v < nvec) {
-      const int c = g * a.cpg + (v * VE) / a.HW;
-      const float ga = to_f32(a.gamma[c]), be = to_f32(a.beta[c]);
-      Pack<T, VE> out;
-#pragma unroll
-      for (int e = 0; e < VE; ++e)
-        out.v[e] = from_f32<T>(sgn_out(to_f32(sv[k].v[e]), K, dmean, rstd, ga, be, a.act));
-      st_stream<T, VE>(a.y + base + static_cast<int64_t>(v) * VE, out);
-    }
+    for (int e = 0; e < VE; ++e)
+      out.v[e] = from_f32<T>(sgn_out(to_f32(sv.v[e]), K, dmean, rstd, ga, be, a.act));
+    st_stream<T, VE>(a.y + base + static_cast<int64_t>(i) * VE, out);
   }
   if (csize > 1) cluster_sync();  // peers may still read slot_m2
 }
@@ -169,11 +198,16 @@ sgn_nchw_resident(const SgnArgs<T, M> a) {
 // blockDim.x = CV * PL with CV = C / VE vectors per pixel: thread t covers the
 // VE channels (t % CV) * VE .. +VE of pixels p0 + t / CV + k * PL, k < NV.
 // CTA b handles batch item b / B, pixels [(b % B) * ppc, +ppc).
-// Dynamic shared memory (floats):
-//   phase 1: cnt[PL] | mean[PL*C] | m2[PL*C]        (per pixel lane, per channel)
-//   phase 3: part[B*groups] as float4, then gmean[groups] | grstd[groups]
-//   tail at k_offset (after the larger of the two, kept throughout): K[groups]
-// Moments are of S - K[g].
+// Inside a CTA the statistics are an exact two-pass over the held S (sums
+// only: per thread, per pixel lane and channel, then per group); across CTAs
+// the (count, mean, M2) partials meet with Chan's merge after one grid
+// barrier.  All moments are of S - K[g], K[g] the group's first residual sum.
+// Dynamic shared memory (floats), layout given by k_offset:
+//   passes:  acc[PL*C] | col[C] | gmean[groups]
+//   merge:   chunk moments[nchunk*groups*3] | gmean[groups] | grstd[groups]
+//   tail at k_offset, kept throughout: K[groups]
+constexpr int kCoopMergeChunk = 8;
+
 template <typename T, typename M, int VE, int NV>
 __global__ void __launch_bounds__(kCoopMaxThreads)
 sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
@@ -209,7 +243,6 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
   float Kl[VE];
 #pragma unroll
   for (int e = 0; e < VE; ++e) Kl[e] = s_K[(c0 + e) / a.cpg];
-  int cnt = 0;
   float lsum[VE];
 #pragma unroll
   for (int e = 0; e < VE; ++e) lsum[e] = 0.0f;
@@ -217,7 +250,6 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
   for (int k = 0; k < NV; ++k) {
     const int p = p0 + tp + k * PL;
     if (p < p1) {
-      ++cnt;
 #pragma unroll
       for (int e = 0; e < VE; ++e) {
         const float sk = a.bcast ? to_f32(skb.v[e]) : to_f32(kv[k].v[e]);
@@ -227,81 +259,86 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
       if (a.s) st_stream<T, VE>(a.s + nbase + static_cast<int64_t>(p) * C + c0, sv[k]);
     }
   }
-  // --- per-thread exact moments of each of its channels ------------------
-  float* s_cnt = smem;
-  float* s_mean = smem + PL;
-  float* s_m2 = s_mean + PL * C;
-  const float fcnt = static_cast<float>(cnt);
+  float* s_acc = smem;
+  float* s_col = smem + PL * C;
+  float* s_gm = s_col + C;
+  const float n_cta = static_cast<float>(p1 - p0) * static_cast<float>(a.cpg);
+
+  // --- pass 1: CTA-local group means of S - K ----------------------------
+#pragma unroll
+  for (int e = 0; e < VE; ++e) s_acc[tp * C + c0 + e] = lsum[e];
+  __syncthreads();
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    float t = 0.0f;
+    for (int q = 0; q < PL; ++q) t += s_acc[q * C + c];
+    s_col[c] = t;
+  }
+  __syncthreads();
+  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
+    float t = 0.0f;
+    for (int cc = 0; cc < a.cpg; ++cc) t += s_col[gg * a.cpg + cc];
+    s_gm[gg] = t / n_cta;
+  }
+  __syncthreads();
+  // --- pass 2: CTA-local sums of squared deviations ----------------------
+  float gml[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) gml[e] = s_gm[(c0 + e) / a.cpg];
 #pragma unroll
   for (int e = 0; e < VE; ++e) {
-    const float mu = cnt ? lsum[e] / fcnt : 0.0f;
     float m2 = 0.0f;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int p = p0 + tp + k * PL;
       if (p < p1) {
-        const float d = (to_f32(sv[k].v[e]) - Kl[e]) - mu;
+        const float d = (to_f32(sv[k].v[e]) - Kl[e]) - gml[e];
         m2 = fmaf(d, d, m2);
       }
     }
-    s_mean[tp * C + c0 + e] = mu;
-    s_m2[tp * C + c0 + e] = m2;
+    s_acc[tp * C + c0 + e] = m2;
   }
-  if (tc == 0) s_cnt[tp] = fcnt;
   __syncthreads();
-  // --- merge pixel lanes per channel (tree over tp, fixed order) ----------
-  for (int stride = 1; stride < PL; stride <<= 1) {
-    for (int idx = threadIdx.x; idx < PL * C; idx += blockDim.x) {
-      const int t = idx / C, c = idx % C;
-      if ((t % (2 * stride)) == 0 && t + stride < PL) {
-        const Moments m = merge(Moments{s_cnt[t], s_mean[t * C + c], s_m2[t * C + c]},
-                                Moments{s_cnt[t + stride], s_mean[(t + stride) * C + c],
-                                        s_m2[(t + stride) * C + c]});
-        s_mean[t * C + c] = m.mean;
-        s_m2[t * C + c] = m.m2;
-      }
-    }
-    __syncthreads();
-    if (threadIdx.x < PL) {
-      const int t = threadIdx.x;
-      if ((t % (2 * stride)) == 0 && t + stride < PL) s_cnt[t] += s_cnt[t + stride];
-    }
-    __syncthreads();
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    float t = 0.0f;
+    for (int q = 0; q < PL; ++q) t += s_acc[q * C + c];
+    s_col[c] = t;
   }
-  // --- merge the channels of each group, publish the CTA's moments --------
+  __syncthreads();
   for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
-    Moments m{0.0f, 0.0f, 0.0f};
-    for (int cc = 0; cc < a.cpg; ++cc) {
-      const int c = gg * a.cpg + cc;
-      m = merge(m, Moments{s_cnt[0], s_mean[c], s_m2[c]});
-    }
-    a.part[static_cast<int64_t>(blockIdx.x) * a.groups + gg] = make_float4(m.n, m.mean, m.m2, 0.0f);
+    float t = 0.0f;
+    for (int cc = 0; cc < a.cpg; ++cc) t += s_col[gg * a.cpg + cc];
+    a.part[static_cast<int64_t>(blockIdx.x) * a.groups + gg] = make_float4(n_cta, s_gm[gg], t, 0.0f);
   }
   __threadfence();
   if (!grid_barrier(a.ctl, gridDim.x, a.limit_ns, 1u)) return;
 
-  // --- merge the batch item's B partials per group (tree, fixed order) ----
-  float4* s_part = smem4;
-  float* s_gmean = reinterpret_cast<float*>(s_part + static_cast<int64_t>(B) * a.groups);
+  // --- merge the batch item's B partials per group ------------------------
+  const int nchunk = (B + kCoopMergeChunk - 1) / kCoopMergeChunk;
+  float* s_cm = smem;                                  // nchunk * groups * 3
+  float* s_gmean = smem + nchunk * a.groups * 3;
   float* s_grstd = s_gmean + a.groups;
   const float4* src = a.part + static_cast<int64_t>(n) * B * a.groups;
-  for (int idx = threadIdx.x; idx < B * a.groups; idx += blockDim.x) s_part[idx] = __ldcg(src + idx);
-  __syncthreads();
-  for (int stride = 1; stride < B; stride <<= 1) {
-    for (int idx = threadIdx.x; idx < B * a.groups; idx += blockDim.x) {
-      const int b = idx / a.groups;
-      if ((b % (2 * stride)) == 0 && b + stride < B) {
-        const float4 u = s_part[idx], w = s_part[idx + stride * a.groups];
-        const Moments m = merge(Moments{u.x, u.y, u.z}, Moments{w.x, w.y, w.z});
-        s_part[idx] = make_float4(m.n, m.mean, m.m2, 0.0f);
-      }
+  for (int idx = threadIdx.x; idx < nchunk * a.groups; idx += blockDim.x) {
+    const int gg = idx % a.groups, q = idx / a.groups;
+    Moments m{0.0f, 0.0f, 0.0f};
+    const int b1 = min(B, (q + 1) * kCoopMergeChunk);
+    for (int b = q * kCoopMergeChunk; b < b1; ++b) {
+      const float4 u = __ldcg(src + static_cast<int64_t>(b) * a.groups + gg);
+      m = merge(m, Moments{u.x, u.y, u.z});
     }
-    __syncthreads();
+    s_cm[idx * 3] = m.n;
+    s_cm[idx * 3 + 1] = m.mean;
+    s_cm[idx * 3 + 2] = m.m2;
   }
+  __syncthreads();
   for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
-    const float4 u = s_part[gg];
-    s_gmean[gg] = u.y;
-    s_grstd[gg] = 1.0f / sqrtf(u.z / u.x + a.eps);
+    Moments m{0.0f, 0.0f, 0.0f};
+    for (int q = 0; q < nchunk; ++q) {
+      const int idx = q * a.groups + gg;
+      m = merge(m, Moments{s_cm[idx * 3], s_cm[idx * 3 + 1], s_cm[idx * 3 + 2]});
+    }
+    s_gmean[gg] = m.mean;
+    s_grstd[gg] = 1.0f / sqrtf(m.m2 / m.n + a.eps);
   }
   __syncthreads();
   // --- normalize what this thread holds -----------------------------------
@@ -519,41 +556,20 @@ static void* pick_coop_any(DType t, DType m, int ve, int nv) {
   return m == DType::F32 ? pick_coop<__half, float>(ve, nv) : pick_coop<__half, __half>(ve, nv);
 }
 
-template <typename T, typename M, int VE, int NV>
-static void* resident_fn() {
-  return reinterpret_cast<void*>(sgn_nchw_resident<T, M, VE, NV>);
-}
-
 template <typename T, typename M>
-static void* pick_resident(int ve, int nv) {
+static void* pick_resident(int ve) {
   constexpr int V16 = static_cast<int>(16 / sizeof(T));
-  if (ve == 1) {
-    switch (nv) {
-      case 1: return resident_fn<T, M, 1, 1>();
-      case 2: return resident_fn<T, M, 1, 2>();
-      case 4: return resident_fn<T, M, 1, 4>();
-      case 8: return resident_fn<T, M, 1, 8>();
-    }
-    return nullptr;
-  }
-  switch (nv) {
-    case 1: return resident_fn<T, M, V16, 1>();
-    case 2: return resident_fn<T, M, V16, 2>();
-    case 4: return resident_fn<T, M, V16, 4>();
-    case 8: return resident_fn<T, M, V16, 8>();
-  }
-  return nullptr;
+  return ve == 1 ? reinterpret_cast<void*>(sgn_nchw_smem<T, M, 1>)
+                 : reinterpret_cast<void*>(sgn_nchw_smem<T, M, V16>);
 }
 
-static void* pick_resident_any(DType t, DType m, int ve, int nv) {
+static void* pick_resident_any(DType t, DType m, int ve) {
   if (t == DType::F32)
-    return m == DType::F32 ? pick_resident<float, float>(ve, nv)
-                           : pick_resident<float, __half>(ve, nv);
-  return m == DType::F32 ? pick_resident<__half, float>(ve, nv)
-                         : pick_resident<__half, __half>(ve, nv);
+    return m == DType::F32 ? pick_resident<float, float>(ve) : pick_resident<float, __half>(ve);
+  return m == DType::F32 ? pick_resident<__half, float>(ve) : pick_resident<__half, __half>(ve);
 }
 
-static bool resident_cluster_fits(void* fn, int block, int csize) {
+static bool resident_cluster_fits(void* fn, int block, int csize, size_t smem) {
   if (csize > 8 &&
       cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
     cudaGetLastError();
@@ -562,6 +578,7 @@ static bool resident_cluster_fits(void* fn, int block, int csize) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize);
   cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = csize;
@@ -577,11 +594,30 @@ static bool resident_cluster_fits(void* fn, int block, int csize) {
   return clusters > 0;
 }
 
+// Set a kernel's dynamic shared memory limit to `smem` if the device allows it.
+static bool allow_smem(void* fn, size_t smem, int dev) {
+  cudaFuncAttributes fa;
+  int optin = 0;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (smem + fa.sharedSizeBytes > static_cast<size_t>(optin)) return false;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+
 // Offset (in floats) of the K[groups] tail of route 2's shared memory.
 static size_t coop_k_offset(int PL, int C, int B, int groups) {
-  const size_t phase1 = static_cast<size_t>(PL) + 2ull * PL * C;
-  const size_t phase3 = static_cast<size_t>(B) * groups * 4 + 2ull * groups;
-  return phase1 > phase3 ? phase1 : phase3;
+  const size_t passes = static_cast<size_t>(PL) * C + C + groups;
+  const size_t nchunk = (static_cast<size_t>(B) + kCoopMergeChunk - 1) / kCoopMergeChunk;
+  const size_t merge = nchunk * groups * 3 + 2ull * groups;
+  return passes > merge ? passes : merge;
 }
 
 static size_t coop_smem_bytes(int PL, int C, int B, int groups) {
@@ -614,39 +650,35 @@ cudaError_t plan_group(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) {
   if (e != cudaSuccess) return e;
 
   if (!c.channels_last) {
-    // Route 1: the instance must fit in one cluster's registers.
+    // Route 1: each CTA stages at most ~40 KB of S in shared memory (five
+    // such CTAs fit an SM), so an instance takes ceil(bytes / 40 KB) CTAs of
+    // a cluster (at most 16); small instances under-filling the GPU are split
+    // further while each CTA keeps at least two vectors per thread.
     const int ve = (vector_ok && HW % vec_elems == 0) ? vec_elems : 1;
     const int64_t nvec = L / ve;
+    const int64_t vbytes = static_cast<int64_t>(ve) * static_cast<int64_t>(dtype_size(c.t));
     const int64_t insts = c.N * c.groups;
-    int best_nv = -1, best_cta = 0, best_cs = 0;
-    for (int cs = 1; cs <= 16 && best_nv < 0; cs *= 2) {
-      for (int nv : {2, 4, 8}) {
-        const int cta = r32(cdiv(nvec, static_cast<int64_t>(nv) * cs));
-        if (cta > kResidentMaxThreads) continue;
-        best_nv = nv;
-        best_cta = cta < 32 ? 32 : cta;
-        best_cs = cs;
-        break;
-      }
+    const int64_t target = 40 * 1024;
+    int64_t cs = cdiv(nvec * vbytes, target);
+    while (cs < 16 && insts * cs < 2LL * sms && cdiv(nvec, cs * 2) >= 2LL * kNchwThreads) cs *= 2;
+    if (cs > 16 || L > 0x7fffffffLL) {
+      *p = two_phase_plan(c);
+      return cudaSuccess;
     }
-    if (best_nv > 0) {
-      // more CTAs per instance when the instances alone under-fill the GPU
-      while (best_cs < 16 && insts * best_cs < 2LL * sms &&
-             r32(cdiv(nvec, static_cast<int64_t>(best_nv) * best_cs * 2)) >= 64) {
-        best_cs *= 2;
-        best_cta = r32(cdiv(nvec, static_cast<int64_t>(best_nv) * best_cs));
-      }
-      void* fn = pick_resident_any(c.t, c.m, ve, best_nv);
-      if (fn && (best_cs == 1 || resident_cluster_fits(fn, best_cta, best_cs)) &&
-          insts * best_cs <= 0x7fffffffLL) {
-        p->route = 1;
-        p->ve = ve;
-        p->nv = best_nv;
-        p->block = best_cta;
-        p->csize = best_cs;
-        p->grid = insts * best_cs;
-        return cudaSuccess;
-      }
+    const int span = static_cast<int>(cdiv(nvec, cs));
+    const size_t smem = static_cast<size_t>(span) * vbytes;
+    void* fn = pick_resident_any(c.t, c.m, ve);
+    if (fn && allow_smem(fn, smem, dev) &&
+        (cs == 1 || resident_cluster_fits(fn, kNchwThreads, static_cast<int>(cs), smem)) &&
+        insts * cs <= 0x7fffffffLL) {
+      p->route = 1;
+      p->ve = ve;
+      p->nv = span;  // vectors per CTA
+      p->block = kNchwThreads;
+      p->csize = static_cast<int>(cs);
+      p->grid = insts * cs;
+      p->smem = smem;
+      return cudaSuccess;
     }
     *p = two_phase_plan(c);
     return cudaSuccess;
@@ -749,7 +781,7 @@ static cudaError_t launch_group_typed(const SkipGroupCall& c, const GroupPlan& p
   cudaLaunchAttribute attr[1];
 
   if (p.route == 1) {
-    void* fn = pick_resident<T, M>(p.ve, p.nv);
+    void* fn = pick_resident<T, M>(p.ve);
     if (!fn) return cudaErrorInvalidConfiguration;
     if (p.csize > 1) {
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -759,7 +791,9 @@ static cudaError_t launch_group_typed(const SkipGroupCall& c, const GroupPlan& p
       cfg.attrs = attr;
       cfg.numAttrs = 1;
     }
-    void* args[] = {&a};
+    int span = p.nv;
+    FastDiv vpc = make_fastdiv(static_cast<unsigned>(a.HW / p.ve));
+    void* args[] = {&a, &span, &vpc};
     return cudaLaunchKernelExC(&cfg, fn, args);
   }
   if (p.route == 2) {

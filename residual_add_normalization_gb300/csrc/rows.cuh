@@ -6,12 +6,12 @@
 // in registers while its sum of squares is reduced, then normalized and
 // written.  Three schedules:
 //
-//   rows_kernel, tpr <= 32   lane groups of `tpr` threads (a power of two) per
-//                            row, several rows per warp, RPG rows per lane group
-//                            in flight; the reduction is a segmented butterfly
-//                            over the low lane bits (no shared memory, no
-//                            barrier).
-//   rows_kernel, tpr  > 32   one row per CTA, or per thread-block cluster for
+//   rows_lane_kernel         lane groups of `tpr` <= 32 threads (a power of two)
+//                            per row, several rows per warp, RPG rows per lane
+//                            group in flight, persistent grid; the reduction is
+//                            a segmented butterfly over the low lane bits (no
+//                            shared memory, no barrier).
+//   rows_cta_kernel          one row per CTA, or per thread-block cluster for
 //                            long rows: warp butterflies, a shared-memory
 //                            combine, then a DSMEM combine across the cluster.
 //   rows_walk_kernel         rows longer than a cluster holds: one CTA walks
@@ -40,6 +40,7 @@ struct SkipRmsArgs {
   float* __restrict__ inv_std; // may be null
   int64_t rows;
   int n;                       // hidden
+  float inv_n;                 // 1 / hidden
   float eps;
 };
 
@@ -51,13 +52,21 @@ struct GatedArgs {
   T* __restrict__ y;
   int64_t rows;
   int n;                       // C
+  float inv_n;                 // 1 / C
   float eps;
 };
+
+// 1 / sqrt(mean square + eps) from a row's sum of squares.
+__device__ __forceinline__ float row_rstd(float sumsq, float inv_n, float eps) {
+  return rsqrtf(fmaf(sumsq, inv_n, eps));
+}
 
 // ---------------------------------------------------------------------------
 // SkipSimplifiedLayerNormalization
 //   S = round_T((x + skip) + bias); y = round_T(S * rstd * gamma),
 //   rstd = 1 / sqrt(sum(S^2) / n + eps)
+// Per-vector weights (gamma, bias) are loaded once per thread and reused for
+// every row the thread handles.
 // ---------------------------------------------------------------------------
 template <typename T, int VE, bool HAS_BIAS, bool WANT_S>
 struct SkipRmsOp {
@@ -67,7 +76,15 @@ struct SkipRmsOp {
   struct In {
     P x, k;
   };
+  struct Wt {
+    P gamma, bias;
+  };
   using Hold = P;
+
+  __device__ static __forceinline__ void load_wt(const Args& a, int v, Wt& w) {
+    w.gamma = ld_reuse<T, VE>(a.gamma + v * VE);
+    if constexpr (HAS_BIAS) w.bias = ld_reuse<T, VE>(a.bias + v * VE);
+  }
 
   __device__ static __forceinline__ void load(const Args& a, int64_t row, int v, In& in) {
     const int64_t off = row * a.n + static_cast<int64_t>(v) * VE;
@@ -77,30 +94,53 @@ struct SkipRmsOp {
 
   template <bool STORE_S = WANT_S>
   __device__ static __forceinline__ float combine(const Args& a, int64_t row, int v,
-                                                  const In& in, Hold& h) {
-    P b;
-    if constexpr (HAS_BIAS) b = ld_reuse<T, VE>(a.bias + v * VE);
+                                                  const In& in, const Wt& w, Hold& h) {
     float ss = 0.0f;
+    if constexpr (VE % 2 == 0) {
 #pragma unroll
-    for (int e = 0; e < VE; ++e) {
-      h.v[e] = residual_sum<T, HAS_BIAS>(in.x.v[e], in.k.v[e], HAS_BIAS ? b.v[e] : T());
-      const float f = to_f32(h.v[e]);
-      ss = fmaf(f, f, ss);
+      for (int i = 0; i < VE / 2; ++i) {
+        const float2 xf = get2(in.x, i), kf = get2(in.k, i);
+        float t0 = __fadd_rn(xf.x, kf.x), t1 = __fadd_rn(xf.y, kf.y);
+        if constexpr (HAS_BIAS) {
+          const float2 bf = get2(w.bias, i);
+          t0 = __fadd_rn(t0, bf.x);
+          t1 = __fadd_rn(t1, bf.y);
+        }
+        set2(h, i, t0, t1);  // one rounding to T
+        const float2 sf = get2(h, i);
+        ss = fmaf(sf.x, sf.x, ss);
+        ss = fmaf(sf.y, sf.y, ss);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        h.v[e] = residual_sum<T, HAS_BIAS>(in.x.v[e], in.k.v[e], HAS_BIAS ? w.bias.v[e] : T());
+        const float f = to_f32(h.v[e]);
+        ss = fmaf(f, f, ss);
+      }
     }
     if constexpr (STORE_S) st_stream<T, VE>(a.s + row * a.n + static_cast<int64_t>(v) * VE, h);
     return ss;
   }
 
   __device__ static __forceinline__ float rstd(const Args& a, float sumsq) {
-    return 1.0f / sqrtf(sumsq / static_cast<float>(a.n) + a.eps);
+    return row_rstd(sumsq, a.inv_n, a.eps);
   }
 
   __device__ static __forceinline__ void finish(const Args& a, int64_t row, int v,
-                                                const Hold& h, float r) {
-    const P g = ld_reuse<T, VE>(a.gamma + v * VE);
+                                                const Hold& h, const Wt& w, float r) {
     P out;
+    if constexpr (VE % 2 == 0) {
 #pragma unroll
-    for (int e = 0; e < VE; ++e) out.v[e] = from_f32<T>(to_f32(h.v[e]) * r * to_f32(g.v[e]));
+      for (int i = 0; i < VE / 2; ++i) {
+        const float2 sf = get2(h, i), gf = get2(w.gamma, i);
+        set2(out, i, sf.x * r * gf.x, sf.y * r * gf.y);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VE; ++e)
+        out.v[e] = from_f32<T>(to_f32(h.v[e]) * r * to_f32(w.gamma.v[e]));
+    }
     st_stream<T, VE>(a.y + row * a.n + static_cast<int64_t>(v) * VE, out);
   }
 
@@ -122,7 +162,14 @@ struct GatedOp {
   struct In {
     P x, g;
   };
+  struct Wt {
+    P scale;
+  };
   using Hold = In;
+
+  __device__ static __forceinline__ void load_wt(const Args& a, int v, Wt& w) {
+    w.scale = ld_reuse<T, VE>(a.scale + v * VE);
+  }
 
   __device__ static __forceinline__ void load(const Args& a, int64_t row, int v, In& in) {
     const int64_t off = row * a.n + static_cast<int64_t>(v) * VE;
@@ -132,29 +179,41 @@ struct GatedOp {
 
   template <bool STORE_S = false>
   __device__ static __forceinline__ float combine(const Args&, int64_t, int, const In& in,
-                                                  Hold& h) {
+                                                  const Wt&, Hold& h) {
     h = in;
     float ss = 0.0f;
+    if constexpr (VE % 2 == 0) {
 #pragma unroll
-    for (int e = 0; e < VE; ++e) {
-      const float f = to_f32(in.x.v[e]);
-      ss = fmaf(f, f, ss);
+      for (int i = 0; i < VE / 2; ++i) {
+        const float2 xf = get2(in.x, i);
+        ss = fmaf(xf.x, xf.x, ss);
+        ss = fmaf(xf.y, xf.y, ss);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) ss = fmaf(to_f32(in.x.v[e]), to_f32(in.x.v[e]), ss);
     }
     return ss;
   }
 
   __device__ static __forceinline__ float rstd(const Args& a, float sumsq) {
-    return 1.0f / sqrtf(sumsq / static_cast<float>(a.n) + a.eps);
+    return row_rstd(sumsq, a.inv_n, a.eps);
   }
 
   __device__ static __forceinline__ void finish(const Args& a, int64_t row, int v,
-                                                const Hold& h, float r) {
-    const P sc = ld_reuse<T, VE>(a.scale + v * VE);
+                                                const Hold& h, const Wt& w, float r) {
     P out;
+    if constexpr (VE % 2 == 0) {
 #pragma unroll
-    for (int e = 0; e < VE; ++e) {
-      const float z = to_f32(h.x.v[e]) * r * to_f32(sc.v[e]);
-      out.v[e] = from_f32<T>(z * silu_f32(to_f32(h.g.v[e])));
+      for (int i = 0; i < VE / 2; ++i) {
+        const float2 xf = get2(h.x, i), gf = get2(h.g, i), sc = get2(w.scale, i);
+        set2(out, i, xf.x * r * sc.x * silu_f32(gf.x), xf.y * r * sc.y * silu_f32(gf.y));
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VE; ++e)
+        out.v[e] = from_f32<T>(to_f32(h.x.v[e]) * r * to_f32(w.scale.v[e]) *
+                               silu_f32(to_f32(h.g.v[e])));
     }
     st_stream<T, VE>(a.y + row * a.n + static_cast<int64_t>(v) * VE, out);
   }
@@ -167,24 +226,41 @@ struct GatedOp {
 // ---------------------------------------------------------------------------
 constexpr int kRowsMaxThreads = 512;
 
-// tpr <= 32: lane groups of tpr threads, RPG rows per lane group per CTA.
-// tpr  > 32: tpr == blockDim.x * cluster size, one row per CTA / cluster, RPG == 1.
-// nvec: vectors of Op::kVE elements per row.  Each thread holds up to NV
-// vectors per row (nvec <= NV * tpr).
-template <class Op, int NV, int RPG>
-__global__ void __launch_bounds__(kRowsMaxThreads)
-rows_kernel(const typename Op::Args a, int tpr, int nvec) {
-  __shared__ float red[33];
-  __shared__ float cl_slot;
-  typename Op::In in[RPG][NV];
-  typename Op::Hold h[RPG][NV];
-  float part[RPG];
+constexpr int kLaneBlock = 256;     // threads per CTA of the lane-group schedule
+#ifndef B200NORM_LANE_MIN_BLOCKS
+#define B200NORM_LANE_MIN_BLOCKS 4
+#endif
+// Resident CTAs per SM the lane-group kernel is compiled for: fewer when each
+// thread holds more vectors in flight (NV * RPG), so those keep their registers.
+constexpr int lane_min_blocks(int held) {
+  return held <= 2 ? B200NORM_LANE_MIN_BLOCKS : (B200NORM_LANE_MIN_BLOCKS + 1) / 2;
+}
 
-  if (tpr <= 32) {
-    const int lane = threadIdx.x & (tpr - 1);
-    const int group = threadIdx.x / tpr;
-    const int groups_per_cta = blockDim.x / tpr;
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * groups_per_cta * RPG + group;
+// Lane-group schedule (tpr <= 32 threads per row, a power of two).  The grid
+// is persistent: CTA b takes row blocks b, b + gridDim.x, ... of
+// (kLaneBlock / tpr) * RPG rows each; lane group g of the CTA takes rows
+// g + i * (kLaneBlock / tpr), i < RPG, of a block, so each step covers
+// consecutive rows.  Per-vector weights stay in registers across blocks.
+// nvec: vectors of Op::kVE elements per row, nvec <= NV * tpr.
+template <class Op, int NV, int RPG>
+__global__ void __launch_bounds__(kLaneBlock, lane_min_blocks(NV * RPG))
+rows_lane_kernel(const typename Op::Args a, int tpr, int nvec) {
+  typename Op::Wt w[NV];
+  const int lane = threadIdx.x & (tpr - 1);
+  const int group = threadIdx.x / tpr;
+  const int groups_per_cta = kLaneBlock / tpr;
+  const int64_t rows_per_block = static_cast<int64_t>(groups_per_cta) * RPG;
+  const int64_t nblocks = (a.rows + rows_per_block - 1) / rows_per_block;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int v = lane + k * tpr;
+    if (v < nvec) Op::load_wt(a, v, w[k]);
+  }
+  for (int64_t blk = blockIdx.x; blk < nblocks; blk += gridDim.x) {
+    typename Op::In in[RPG][NV];
+    typename Op::Hold h[RPG][NV];
+    float part[RPG];
+    const int64_t base = blk * rows_per_block + group;
 #pragma unroll
     for (int i = 0; i < RPG; ++i) {
       const int64_t row = base + static_cast<int64_t>(i) * groups_per_cta;
@@ -201,7 +277,7 @@ rows_kernel(const typename Op::Args a, int tpr, int nvec) {
 #pragma unroll
       for (int k = 0; k < NV; ++k) {
         const int v = lane + k * tpr;
-        if (row < a.rows && v < nvec) part[i] += Op::combine(a, row, v, in[i][k], h[i][k]);
+        if (row < a.rows && v < nvec) part[i] += Op::combine(a, row, v, in[i][k], w[k], h[i][k]);
       }
     }
 #pragma unroll
@@ -212,14 +288,22 @@ rows_kernel(const typename Op::Args a, int tpr, int nvec) {
 #pragma unroll
       for (int k = 0; k < NV; ++k) {
         const int v = lane + k * tpr;
-        if (v < nvec) Op::finish(a, row, v, h[i][k], r);
+        if (v < nvec) Op::finish(a, row, v, h[i][k], w[k], r);
       }
       if (lane == 0) Op::row_stats(a, row, r);
     }
-    return;
   }
+}
 
-  // One row per CTA or per cluster.
+// One row per CTA, or per cluster of CTAs (tpr == blockDim.x * cluster size).
+// Weights are loaded where they are used (they are L1/L2 hits).
+template <class Op, int NV>
+__global__ void __launch_bounds__(kRowsMaxThreads)
+rows_cta_kernel(const typename Op::Args a, int tpr, int nvec) {
+  __shared__ float red[33];
+  __shared__ float cl_slot;
+  typename Op::In in[NV];
+  typename Op::Hold h[NV];
   const unsigned csize = cluster_size();
   const unsigned rank = csize > 1 ? cluster_rank() : 0u;
   const int64_t row = blockIdx.x / csize;
@@ -227,13 +311,17 @@ rows_kernel(const typename Op::Args a, int tpr, int nvec) {
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int v = first + k * tpr;
-    if (v < nvec) Op::load(a, row, v, in[0][k]);
+    if (v < nvec) Op::load(a, row, v, in[k]);
   }
   float acc = 0.0f;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int v = first + k * tpr;
-    if (v < nvec) acc += Op::combine(a, row, v, in[0][k], h[0][k]);
+    if (v < nvec) {
+      typename Op::Wt w;
+      Op::load_wt(a, v, w);
+      acc += Op::combine(a, row, v, in[k], w, h[k]);
+    }
   }
   float total = cta_sum(acc, red);
   if (csize > 1) total = cluster_sum(total, &cl_slot, csize);
@@ -241,7 +329,11 @@ rows_kernel(const typename Op::Args a, int tpr, int nvec) {
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int v = first + k * tpr;
-    if (v < nvec) Op::finish(a, row, v, h[0][k], r);
+    if (v < nvec) {
+      typename Op::Wt w;
+      Op::load_wt(a, v, w);
+      Op::finish(a, row, v, h[k], w, r);
+    }
   }
   if (first == 0) Op::row_stats(a, row, r);
   if (csize > 1) cluster_sync();  // peers may still read cl_slot
@@ -259,16 +351,20 @@ rows_walk_kernel(const typename Op::Args a, int nvec) {
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     typename Op::In in;
     typename Op::Hold h;
+    typename Op::Wt w;
+    Op::load_wt(a, v, w);
     Op::load(a, row, v, in);
-    acc += Op::combine(a, row, v, in, h);
+    acc += Op::combine(a, row, v, in, w, h);
   }
   const float r = Op::rstd(a, cta_sum(acc, red));
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     typename Op::In in;
     typename Op::Hold h;
+    typename Op::Wt w;
+    Op::load_wt(a, v, w);
     Op::load(a, row, v, in);
-    Op::template combine<false>(a, row, v, in, h);
-    Op::finish(a, row, v, h, r);
+    Op::template combine<false>(a, row, v, in, w, h);
+    Op::finish(a, row, v, h, w, r);
   }
   if (threadIdx.x == 0) Op::row_stats(a, row, r);
 }

@@ -8,9 +8,6 @@
 #ifndef B200NORM_CTA_NV
 #define B200NORM_CTA_NV 4      // vectors per thread for CTA-per-row schedules
 #endif
-#ifndef B200NORM_PACKED_BLOCK
-#define B200NORM_PACKED_BLOCK 256
-#endif
 
 namespace b200norm {
 
@@ -36,14 +33,14 @@ RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok) {
     p.tpr = pow2_ceil(nvec);
     p.nv = 1;
     p.rpg = p.tpr <= 16 ? B200NORM_SHORT_RPG : 1;
-    p.block = B200NORM_PACKED_BLOCK;
+    p.block = kLaneBlock;
     p.grid = ceil_div(rows, static_cast<int64_t>(p.block / p.tpr) * p.rpg);
   } else if (nvec <= 128) {
     // Warp per row, up to four vectors per lane.
     p.mode = 0;
     p.tpr = 32;
     p.nv = pow2_ceil(ceil_div(nvec, 32));
-    p.block = B200NORM_PACKED_BLOCK;
+    p.block = kLaneBlock;
     p.grid = ceil_div(rows, p.block / 32);
   } else {
     // CTA per row; a cluster per row once one CTA cannot hold it.

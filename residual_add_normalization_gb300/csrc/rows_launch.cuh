@@ -9,26 +9,35 @@ namespace b200norm {
 template <class Op>
 using RowsKernelFn = void (*)(const typename Op::Args, int, int);
 
-// The (NV, RPG) instantiations every Op provides.
+// Lane-group instantiations: (NV, RPG) in {(1,1), (1,2), (1,4), (2,1), (4,1)}.
 template <class Op>
-RowsKernelFn<Op> pick_rows_kernel(int nv, int rpg) {
-  if (rpg == 1) {
-    switch (nv) {
-      case 1: return rows_kernel<Op, 1, 1>;
-      case 2: return rows_kernel<Op, 2, 1>;
-      case 4: return rows_kernel<Op, 4, 1>;
-      case 8: return rows_kernel<Op, 8, 1>;
-      default: return nullptr;
-    }
-  }
+RowsKernelFn<Op> pick_lane_kernel(int nv, int rpg) {
   if (nv == 1) {
     switch (rpg) {
-      case 2: return rows_kernel<Op, 1, 2>;
-      case 4: return rows_kernel<Op, 1, 4>;
+      case 1: return rows_lane_kernel<Op, 1, 1>;
+      case 2: return rows_lane_kernel<Op, 1, 2>;
+      case 4: return rows_lane_kernel<Op, 1, 4>;
       default: return nullptr;
     }
   }
-  return nullptr;
+  if (rpg != 1) return nullptr;
+  switch (nv) {
+    case 2: return rows_lane_kernel<Op, 2, 1>;
+    case 4: return rows_lane_kernel<Op, 4, 1>;
+    default: return nullptr;
+  }
+}
+
+// CTA / cluster instantiations: NV in {1, 2, 4, 8}.
+template <class Op>
+RowsKernelFn<Op> pick_cta_kernel(int nv) {
+  switch (nv) {
+    case 1: return rows_cta_kernel<Op, 1>;
+    case 2: return rows_cta_kernel<Op, 2>;
+    case 4: return rows_cta_kernel<Op, 4>;
+    case 8: return rows_cta_kernel<Op, 8>;
+    default: return nullptr;
+  }
 }
 
 template <class Op>
@@ -38,11 +47,22 @@ cudaError_t launch_rows_op(const typename Op::Args& a, const RowPlan& p, cudaStr
     rows_walk_kernel<Op><<<static_cast<unsigned>(p.grid), p.block, 0, stream>>>(a, nvec);
     return cudaGetLastError();
   }
-  RowsKernelFn<Op> fn = pick_rows_kernel<Op>(p.nv, p.rpg);
+  RowsKernelFn<Op> fn = p.mode == 0 ? pick_lane_kernel<Op>(p.nv, p.rpg) : pick_cta_kernel<Op>(p.nv);
   if (!fn) return cudaErrorInvalidConfiguration;
+  int64_t grid = p.grid;
+  if (p.mode == 0) {
+    // persistent lane-group schedule: as many CTAs as can be resident
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kLaneBlock, 0);
+    if (e != cudaSuccess) return e;
+    const int64_t resident = static_cast<int64_t>(per_sm > 0 ? per_sm : 1) * sms;
+    if (grid > resident) grid = resident;
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
-  cfg.blockDim = dim3(p.block);
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(p.mode == 0 ? kLaneBlock : p.block);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -64,7 +84,7 @@ cudaError_t launch_rows_op(const typename Op::Args& a, const RowPlan& p, cudaStr
 // Can a cluster of `csize` CTAs of `block` threads of this kernel be resident?
 template <class Op>
 bool cluster_fits(int nv, int block, int csize) {
-  RowsKernelFn<Op> fn = pick_rows_kernel<Op>(nv, 1);
+  RowsKernelFn<Op> fn = pick_cta_kernel<Op>(nv);
   if (!fn) return false;
   if (csize > 8 &&
       cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {

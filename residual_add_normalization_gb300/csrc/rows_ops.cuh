@@ -34,6 +34,7 @@ cudaError_t skip_rms_go(const SkipRmsCall& c, const RowPlan& plan, cudaStream_t 
   a.inv_std = c.inv_std;
   a.rows = c.rows;
   a.n = static_cast<int>(c.hidden);
+  a.inv_n = 1.0f / static_cast<float>(c.hidden);
   a.eps = c.eps;
   return launch_rows_op<Op>(a, settle_plan<Op>(plan, c.rows), st);
 }
@@ -56,6 +57,7 @@ cudaError_t gated_go(const GatedCall& c, const RowPlan& plan, cudaStream_t st) {
   a.y = static_cast<T*>(c.y);
   a.rows = c.rows;
   a.n = static_cast<int>(c.C);
+  a.inv_n = 1.0f / static_cast<float>(c.C);
   a.eps = c.eps;
   return launch_rows_op<Op>(a, settle_plan<Op>(plan, c.rows), st);
 }
