@@ -127,10 +127,27 @@ __device__ __forceinline__ T residual_sum(T x, T skip, T bias) {
   return from_f32<T>(t);
 }
 
-// SiLU in binary32: z * sigmoid(z) = z / (1 + e^-z).  Uses the fast exp and
-// divide intrinsics (a few ulp of binary32, far inside the output tolerance).
+// SiLU in binary32: z * sigmoid(z) = z / (1 + e^-z), with e^-z written as
+// 2^(-z * log2(e)) and evaluated by the hardware base-2 exponential, and the
+// division by the hardware reciprocal (each a few ulp of binary32, far inside
+// the output tolerance).  Flushing subnormals here is harmless: 2^(-z log2 e)
+// is subnormal only for z > 87, where 1 + e^-z rounds to 1 anyway, and the
+// reciprocal's argument is >= 1.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float silu_f32(float z) {
-  return __fdividef(z, 1.0f + __expf(-z));
+  constexpr float kLog2e = 1.4426950408889634f;
+  return z * rcp_approx(1.0f + ex2_approx(-z * kLog2e));
 }
 
 // ---------------------------------------------------------------------------

@@ -26,6 +26,8 @@
 // group (its first residual sum), d the mean of S - K.  S - K is exact for
 // data near the mean, so (S - K) - d stays accurate in binary32 even when
 // |mean| is large against the group's spread.
+#include <cstring>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -205,11 +207,11 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
 // Dynamic shared memory (floats), layout given by k_offset:
 //   passes:  acc[PL*C] | col[C] | gmean[groups]
 //   merge:   chunk moments[nchunk*groups*3] | gmean[groups] | grstd[groups]
-//   tail at k_offset, kept throughout: K[groups]
-constexpr int kCoopMergeChunk = 8;
+//   tail at k_offset, kept throughout: K[groups] | gamma[C] | beta[C]
+constexpr int kCoopMergeChunk = 4;
 
 template <typename T, typename M, int VE, int NV>
-__global__ void __launch_bounds__(kCoopMaxThreads)
+__global__ void __launch_bounds__(kCoopMaxThreads, 1)
 sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
   extern __shared__ float4 smem4[];
   float* smem = reinterpret_cast<float*>(smem4);
@@ -225,7 +227,7 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
   const int64_t nbase = static_cast<int64_t>(n) * a.HW * C;
   const int c0 = tc * VE;
 
-  // --- load and form S --------------------------------------------------
+  // --- load and form S (S is stored after the barrier, with Y) ------------
   Pack<T, VE> xv[NV], kv[NV], sv[NV];
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
@@ -238,6 +240,13 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
   }
   Pack<T, VE> skb;
   if (a.bcast) skb = ld_reuse<T, VE>(a.skip + static_cast<int64_t>(n) * C + c0);
+  // the affine weights are needed only at the end: stage them now
+  float* s_ga = s_K + a.groups;
+  float* s_be = s_ga + C;
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    s_ga[c] = to_f32(__ldg(a.gamma + c));
+    s_be[c] = to_f32(__ldg(a.beta + c));
+  }
   for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) s_K[gg] = sgn_shift(a, n, gg, true);
   __syncthreads();
   float Kl[VE];
@@ -256,9 +265,9 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
         sv[k].v[e] = sgn_sum<T>(to_f32(xv[k].v[e]), sk, a.bias, c0 + e);
         lsum[e] += to_f32(sv[k].v[e]) - Kl[e];
       }
-      if (a.s) st_stream<T, VE>(a.s + nbase + static_cast<int64_t>(p) * C + c0, sv[k]);
     }
   }
+  // acc is laid out [e][tp][tc] so that the stores of a warp hit distinct banks
   float* s_acc = smem;
   float* s_col = smem + PL * C;
   float* s_gm = s_col + C;
@@ -266,12 +275,13 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
 
   // --- pass 1: CTA-local group means of S - K ----------------------------
 #pragma unroll
-  for (int e = 0; e < VE; ++e) s_acc[tp * C + c0 + e] = lsum[e];
+  for (int e = 0; e < VE; ++e) s_acc[(e * PL + tp) * CV + tc] = lsum[e];
   __syncthreads();
-  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+  for (int j = threadIdx.x; j < C; j += blockDim.x) {
+    const int e = j / CV, q0 = j % CV;
     float t = 0.0f;
-    for (int q = 0; q < PL; ++q) t += s_acc[q * C + c];
-    s_col[c] = t;
+    for (int q = 0; q < PL; ++q) t += s_acc[(e * PL + q) * CV + q0];
+    s_col[q0 * VE + e] = t;
   }
   __syncthreads();
   for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
@@ -295,13 +305,14 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
         m2 = fmaf(d, d, m2);
       }
     }
-    s_acc[tp * C + c0 + e] = m2;
+    s_acc[(e * PL + tp) * CV + tc] = m2;
   }
   __syncthreads();
-  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+  for (int j = threadIdx.x; j < C; j += blockDim.x) {
+    const int e = j / CV, q0 = j % CV;
     float t = 0.0f;
-    for (int q = 0; q < PL; ++q) t += s_acc[q * C + c];
-    s_col[c] = t;
+    for (int q = 0; q < PL; ++q) t += s_acc[(e * PL + q) * CV + q0];
+    s_col[q0 * VE + e] = t;
   }
   __syncthreads();
   for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
@@ -309,10 +320,12 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
     for (int cc = 0; cc < a.cpg; ++cc) t += s_col[gg * a.cpg + cc];
     a.part[static_cast<int64_t>(blockIdx.x) * a.groups + gg] = make_float4(n_cta, s_gm[gg], t, 0.0f);
   }
-  __threadfence();
+  __threadfence();  // partials visible GPU-wide before this CTA arrives
   if (!grid_barrier(a.ctl, gridDim.x, a.limit_ns, 1u)) return;
 
   // --- merge the batch item's B partials per group ------------------------
+  // chunks of kCoopMergeChunk partials: all loads of a chunk are issued
+  // before its merges, then the chunk results are merged per group
   const int nchunk = (B + kCoopMergeChunk - 1) / kCoopMergeChunk;
   float* s_cm = smem;                                  // nchunk * groups * 3
   float* s_gmean = smem + nchunk * a.groups * 3;
@@ -320,12 +333,15 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
   const float4* src = a.part + static_cast<int64_t>(n) * B * a.groups;
   for (int idx = threadIdx.x; idx < nchunk * a.groups; idx += blockDim.x) {
     const int gg = idx % a.groups, q = idx / a.groups;
+    const int b0 = q * kCoopMergeChunk;
+    float4 u[kCoopMergeChunk];
+#pragma unroll
+    for (int j = 0; j < kCoopMergeChunk; ++j)
+      if (b0 + j < B) u[j] = __ldcg(src + static_cast<int64_t>(b0 + j) * a.groups + gg);
     Moments m{0.0f, 0.0f, 0.0f};
-    const int b1 = min(B, (q + 1) * kCoopMergeChunk);
-    for (int b = q * kCoopMergeChunk; b < b1; ++b) {
-      const float4 u = __ldcg(src + static_cast<int64_t>(b) * a.groups + gg);
-      m = merge(m, Moments{u.x, u.y, u.z});
-    }
+#pragma unroll
+    for (int j = 0; j < kCoopMergeChunk; ++j)
+      if (b0 + j < B) m = merge(m, Moments{u[j].x, u[j].y, u[j].z});
     s_cm[idx * 3] = m.n;
     s_cm[idx * 3 + 1] = m.mean;
     s_cm[idx * 3 + 2] = m.m2;
@@ -341,26 +357,25 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
     s_grstd[gg] = 1.0f / sqrtf(m.m2 / m.n + a.eps);
   }
   __syncthreads();
-  // --- normalize what this thread holds -----------------------------------
-  float ga[VE], be[VE], mu[VE], rs[VE];
+  // --- normalize what this thread holds; store S and Y ---------------------
+  float mu[VE], rs[VE];
 #pragma unroll
   for (int e = 0; e < VE; ++e) {
-    const int c = c0 + e;
-    ga[e] = to_f32(a.gamma[c]);
-    be[e] = to_f32(a.beta[c]);
-    mu[e] = s_gmean[c / a.cpg];
-    rs[e] = s_grstd[c / a.cpg];
+    mu[e] = s_gmean[(c0 + e) / a.cpg];
+    rs[e] = s_grstd[(c0 + e) / a.cpg];
   }
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int p = p0 + tp + k * PL;
     if (p < p1) {
+      const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+      if (a.s) st_stream<T, VE>(a.s + off, sv[k]);
       Pack<T, VE> out;
 #pragma unroll
       for (int e = 0; e < VE; ++e)
-        out.v[e] = from_f32<T>(
-            sgn_out(to_f32(sv[k].v[e]), Kl[e], mu[e], rs[e], ga[e], be[e], a.act));
-      st_stream<T, VE>(a.y + nbase + static_cast<int64_t>(p) * C + c0, out);
+        out.v[e] = from_f32<T>(sgn_out(to_f32(sv[k].v[e]), Kl[e], mu[e], rs[e],
+                                       s_ga[c0 + e], s_be[c0 + e], a.act));
+      st_stream<T, VE>(a.y + off, out);
     }
   }
 }
@@ -513,7 +528,6 @@ __global__ void barrier_timeout_probe(Control* ctl, unsigned long long limit_ns)
 // Host side
 // ---------------------------------------------------------------------------
 static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
-static int r32(int64_t v) { return static_cast<int>(cdiv(v, 32) * 32); }
 
 size_t group_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int groups) {
   if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || groups <= 0) return kControlBytes;
@@ -621,7 +635,7 @@ static size_t coop_k_offset(int PL, int C, int B, int groups) {
 }
 
 static size_t coop_smem_bytes(int PL, int C, int B, int groups) {
-  return (coop_k_offset(PL, C, B, groups) + groups) * sizeof(float);
+  return (coop_k_offset(PL, C, B, groups) + groups + 2ull * C) * sizeof(float);
 }
 
 GroupPlan two_phase_plan(const SkipGroupCall& c) {
@@ -638,7 +652,38 @@ GroupPlan two_phase_plan(const SkipGroupCall& c) {
   return p;
 }
 
+static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, GroupPlan* p);
+
+// Plans depend on the device, the shape, the types and the alignment only;
+// the occupancy queries behind them are costly, so they are cached.
+struct GroupPlanKey {
+  int dev;
+  int64_t N, C, H, W;
+  int groups, t, m, cl, vec;
+};
+
 cudaError_t plan_group(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) {
+  static PlanCache<GroupPlanKey, GroupPlan> cache;
+  GroupPlanKey k;
+  memset(&k, 0, sizeof(k));
+  cudaError_t e = cudaGetDevice(&k.dev);
+  if (e != cudaSuccess) return e;
+  k.N = c.N;
+  k.C = c.C;
+  k.H = c.H;
+  k.W = c.W;
+  k.groups = c.groups;
+  k.t = static_cast<int>(c.t);
+  k.m = static_cast<int>(c.m);
+  k.cl = c.channels_last ? 1 : 0;
+  k.vec = vector_ok ? 1 : 0;
+  if (cache.get(k, p)) return cudaSuccess;
+  e = plan_group_uncached(c, vector_ok, p);
+  if (e == cudaSuccess) cache.put(k, *p);
+  return e;
+}
+
+static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) {
   *p = GroupPlan{};
   const int64_t HW = c.H * c.W;
   const int64_t cpg = c.C / c.groups;

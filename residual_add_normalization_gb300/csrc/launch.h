@@ -6,8 +6,42 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <string.h>
+
+#include <mutex>
 
 namespace b200norm {
+
+// A small thread-safe cache of launch decisions keyed by a plain struct
+// (compared bytewise: callers zero the key before filling it).  Oldest
+// entries are overwritten once it is full.
+template <class Key, class Val, int N = 64>
+class PlanCache {
+ public:
+  bool get(const Key& k, Val* v) {
+    std::lock_guard<std::mutex> lock(mu_);
+    for (int i = 0; i < N; ++i)
+      if (used_[i] && memcmp(&keys_[i], &k, sizeof(Key)) == 0) {
+        *v = vals_[i];
+        return true;
+      }
+    return false;
+  }
+  void put(const Key& k, const Val& v) {
+    std::lock_guard<std::mutex> lock(mu_);
+    keys_[next_] = k;
+    vals_[next_] = v;
+    used_[next_] = true;
+    next_ = (next_ + 1) % N;
+  }
+
+ private:
+  std::mutex mu_;
+  Key keys_[N];
+  Val vals_[N];
+  bool used_[N] = {};
+  int next_ = 0;
+};
 
 enum class DType { F32 = 0, F16 = 1 };
 

@@ -228,12 +228,12 @@ constexpr int kRowsMaxThreads = 512;
 
 constexpr int kLaneBlock = 256;     // threads per CTA of the lane-group schedule
 #ifndef B200NORM_LANE_MIN_BLOCKS
-#define B200NORM_LANE_MIN_BLOCKS 4
+#define B200NORM_LANE_MIN_BLOCKS 8
 #endif
 // Resident CTAs per SM the lane-group kernel is compiled for: fewer when each
 // thread holds more vectors in flight (NV * RPG), so those keep their registers.
 constexpr int lane_min_blocks(int held) {
-  return held <= 2 ? B200NORM_LANE_MIN_BLOCKS : (B200NORM_LANE_MIN_BLOCKS + 1) / 2;
+  return B200NORM_LANE_MIN_BLOCKS / held > 0 ? B200NORM_LANE_MIN_BLOCKS / held : 1;
 }
 
 // Lane-group schedule (tpr <= 32 threads per row, a power of two).  The grid

@@ -3,7 +3,10 @@
 #include "rows_ops.cuh"
 
 #ifndef B200NORM_SHORT_RPG
-#define B200NORM_SHORT_RPG 2   // rows per lane group for spans of <= 16 vectors
+#define B200NORM_SHORT_RPG 1   // rows per lane group for spans of <= 32 vectors
+#endif
+#ifndef B200NORM_SHORT_NV
+#define B200NORM_SHORT_NV 1    // vectors per thread for spans of <= 32 vectors
 #endif
 #ifndef B200NORM_CTA_NV
 #define B200NORM_CTA_NV 4      // vectors per thread for CTA-per-row schedules
@@ -30,9 +33,9 @@ RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok) {
   if (nvec <= 32) {
     // Short spans: a power-of-two lane group per row, several rows per warp.
     p.mode = 0;
-    p.tpr = pow2_ceil(nvec);
-    p.nv = 1;
-    p.rpg = p.tpr <= 16 ? B200NORM_SHORT_RPG : 1;
+    p.nv = nvec >= B200NORM_SHORT_NV ? B200NORM_SHORT_NV : 1;
+    p.tpr = pow2_ceil(ceil_div(nvec, p.nv));
+    p.rpg = p.nv == 1 && p.tpr <= 16 ? B200NORM_SHORT_RPG : 1;
     p.block = kLaneBlock;
     p.grid = ceil_div(rows, static_cast<int64_t>(p.block / p.tpr) * p.rpg);
   } else if (nvec <= 128) {

@@ -9,6 +9,30 @@ namespace b200norm {
 template <class Op>
 using RowsKernelFn = void (*)(const typename Op::Args, int, int);
 
+// CTAs of `block` threads of kernel `fn` that the current device holds at
+// once (cached per device and kernel).
+inline cudaError_t resident_ctas(const void* fn, int block, int64_t* out) {
+  struct Key {
+    int dev, block;
+    const void* fn;
+  };
+  static PlanCache<Key, int64_t> cache;
+  Key k;
+  memset(&k, 0, sizeof(k));
+  cudaError_t e = cudaGetDevice(&k.dev);
+  if (e != cudaSuccess) return e;
+  k.block = block;
+  k.fn = fn;
+  if (cache.get(k, out)) return cudaSuccess;
+  int sms = 0, per_sm = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, k.dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, block, 0);
+  if (e != cudaSuccess) return e;
+  *out = static_cast<int64_t>(per_sm > 0 ? per_sm : 1) * sms;
+  cache.put(k, *out);
+  return cudaSuccess;
+}
+
 // Lane-group instantiations: (NV, RPG) in {(1,1), (1,2), (1,4), (2,1), (4,1)}.
 template <class Op>
 RowsKernelFn<Op> pick_lane_kernel(int nv, int rpg) {
@@ -52,12 +76,9 @@ cudaError_t launch_rows_op(const typename Op::Args& a, const RowPlan& p, cudaStr
   int64_t grid = p.grid;
   if (p.mode == 0) {
     // persistent lane-group schedule: as many CTAs as can be resident
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kLaneBlock, 0);
+    int64_t resident = 0;
+    cudaError_t e = resident_ctas(reinterpret_cast<const void*>(fn), kLaneBlock, &resident);
     if (e != cudaSuccess) return e;
-    const int64_t resident = static_cast<int64_t>(per_sm > 0 ? per_sm : 1) * sms;
     if (grid > resident) grid = resident;
   }
   cudaLaunchConfig_t cfg = {};
@@ -81,11 +102,8 @@ cudaError_t launch_rows_op(const typename Op::Args& a, const RowPlan& p, cudaStr
   return cudaLaunchKernelEx(&cfg, fn, a, p.tpr, nvec);
 }
 
-// Can a cluster of `csize` CTAs of `block` threads of this kernel be resident?
 template <class Op>
-bool cluster_fits(int nv, int block, int csize) {
-  RowsKernelFn<Op> fn = pick_cta_kernel<Op>(nv);
-  if (!fn) return false;
+bool cluster_fits_query(RowsKernelFn<Op> fn, int block, int csize) {
   if (csize > 8 &&
       cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
     cudaGetLastError();
@@ -108,5 +126,33 @@ bool cluster_fits(int nv, int block, int csize) {
   }
   return clusters > 0;
 }
+
+// Can a cluster of `csize` CTAs of `block` threads of this kernel be resident?
+// (cached per device and configuration)
+template <class Op>
+bool cluster_fits(int nv, int block, int csize) {
+  RowsKernelFn<Op> fn = pick_cta_kernel<Op>(nv);
+  if (!fn) return false;
+  struct Key {
+    int dev, block, csize;
+    const void* fn;
+  };
+  static PlanCache<Key, bool> cache;
+  Key k;
+  memset(&k, 0, sizeof(k));
+  if (cudaGetDevice(&k.dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  k.block = block;
+  k.csize = csize;
+  k.fn = reinterpret_cast<const void*>(fn);
+  bool fits = false;
+  if (cache.get(k, &fits)) return fits;
+  fits = cluster_fits_query<Op>(fn, block, csize);
+  cache.put(k, fits);
+  return fits;
+}
+
 
 }  // namespace b200norm

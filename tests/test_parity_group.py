@@ -69,6 +69,8 @@ NCHW_CASES = [
     (1, 320, 64, 64, 32),   # 40,960-element instances: clusters
     (1, 64, 128, 128, 1),   # one 1M-element instance: two-phase
     (4, 6, 1, 1, 6),        # one element per group
+    (6, 256, 8, 8, 32),     # 192 instances, more than one per SM
+    (5, 96, 12, 12, 32),    # 160 instances of 432 elements
 ]
 
 
