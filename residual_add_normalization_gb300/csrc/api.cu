@@ -289,7 +289,11 @@ b200norm_status b200norm_skip_group(const void* x, const void* skip, int skip_ra
   if (g_force_group_route == 3) plan = two_phase_plan(c);
   if (plan.grid > kMaxGrid) return fail(B200NORM_ERR_UNSUPPORTED, "problem too large for one launch");
   e = launch_group(c, plan, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "skip_group launch");
+  if (e != cudaSuccess)
+    return fail(B200NORM_ERR_CUDA,
+                "skip_group launch (route %d, grid %lld, block %d, cluster %d, smem %zu): %s",
+                plan.route, static_cast<long long>(plan.grid), plan.block, plan.csize, plan.smem,
+                cudaGetErrorString(e));
   return ok();
 }
 

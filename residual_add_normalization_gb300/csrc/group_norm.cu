@@ -608,7 +608,10 @@ static bool resident_cluster_fits(void* fn, int block, int csize, size_t smem) {
   return clusters > 0;
 }
 
-// Set a kernel's dynamic shared memory limit to `smem` if the device allows it.
+// Can kernel `fn` take `smem` bytes of dynamic shared memory on device `dev`?
+// The kernel's limit is raised to everything the device allows next to its
+// static shared memory (never lowered), so that plans cached for this kernel
+// with different sizes all stay launchable.
 static bool allow_smem(void* fn, size_t smem, int dev) {
   cudaFuncAttributes fa;
   int optin = 0;
@@ -617,9 +620,10 @@ static bool allow_smem(void* fn, size_t smem, int dev) {
     cudaGetLastError();
     return false;
   }
-  if (smem + fa.sharedSizeBytes > static_cast<size_t>(optin)) return false;
+  const size_t cap = static_cast<size_t>(optin) - fa.sharedSizeBytes;
+  if (smem > cap) return false;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess) {
+                           static_cast<int>(cap)) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }

@@ -1,8 +1,8 @@
 """GPU parity: SkipGroupNorm kernels against the CPU oracle on the same seeded
 inputs, through the C ABI (via the binding).
 
-Covers the three routes (NCHW resident CTA / cluster per group instance, NHWC
-cooperative grid with a bounded grid barrier, two-phase for anything else),
+Covers the three routes (NCHW: CTA / cluster per group instance; NHWC: a
+cooperative grid with one bounded grid barrier; two-phase for anything else),
 both layouts, both T and both M, full / (N, C) / (N, 1, 1, C) skip, bias and S
 on and off, SiLU on and off, vector and scalar paths, and ragged slabs.
 """
@@ -93,8 +93,10 @@ NHWC_CASES = [
     (3, 5, 7, 12, 3),       # C % 8 != 0: scalar path
     (1, 33, 17, 40, 8),     # ragged last slab
     (2, 16, 16, 4104, 8),   # C / 8 = 513 vectors per pixel: two-phase
-    (600, 2, 2, 16, 4),     # more batch items than resident CTAs: two-phase
+    (600, 2, 2, 16, 4),     # many batch items
     (4, 1, 1, 6, 6),
+    (1, 256, 256, 64, 1),   # one 4M-element group
+    (2, 64, 64, 96, 24),    # cpg 4: 8-channel vectors span two groups
 ]
 
 
