@@ -294,14 +294,39 @@ def run_ours(args, rank, world, dist):
               if v is not None)
     d2h = sum(o.numel() * o.element_size() for c in calls for o in c["outs"])
 
+    # Three streams: host->device copies of each operator's inputs, the
+    # operator calls (public API on the compute stream), device->host copies
+    # of its outputs.  Events order each operator after its inputs, each
+    # download after its operator, and each reuse of a device buffer after
+    # the previous step's use of it, so uploads, compute and downloads of
+    # different operators overlap.
+    s_up, s_comp, s_down = (torch.cuda.Stream(dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in calls]
+    ev_done = [torch.cuda.Event() for _ in calls]
+    ev_out = [torch.cuda.Event() for _ in calls]
+    first = [True]
+
     def e2e_step():
-        for c, pin, pout in zip(calls, pinned_in, pinned_out):
-            for k, v in pin.items():
-                if v is not None:
-                    c["inputs"][k].copy_(v, non_blocking=True)
-            c["fn"]()
-            for o, p in zip(c["outs"], pout):
-                p.copy_(o, non_blocking=True)
+        for i, (c, pin, pout) in enumerate(zip(calls, pinned_in, pinned_out)):
+            with torch.cuda.stream(s_up):
+                if not first[0]:
+                    s_up.wait_event(ev_done[i])  # previous step no longer reads them
+                for k, v in pin.items():
+                    if v is not None:
+                        c["inputs"][k].copy_(v, non_blocking=True)
+                ev_in[i].record(s_up)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(ev_in[i])
+                if not first[0]:
+                    s_comp.wait_event(ev_out[i])  # previous outputs downloaded
+                c["fn"]()
+                ev_done[i].record(s_comp)
+            with torch.cuda.stream(s_down):
+                s_down.wait_event(ev_done[i])
+                for o, p in zip(c["outs"], pout):
+                    p.copy_(o, non_blocking=True)
+                ev_out[i].record(s_down)
+        first[0] = False
 
     e2e_ms = float("nan")
     if e2e_steps:
@@ -312,15 +337,19 @@ def run_ours(args, rank, world, dist):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        for st in (s_up, s_comp, s_down):
+            st.wait_event(e0)
         for _ in range(e2e_steps):
             e2e_step()
+        for st in (s_up, s_comp, s_down):
+            stream.wait_stream(st)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+        if dist:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
 
     if rank != 0:
         return None

@@ -28,6 +28,21 @@ B200NORM_API b200norm_status b200norm_testing_barrier_timeout(void* workspace,
  * Other values are rejected with B200NORM_ERR_INVALID_ARGUMENT. */
 B200NORM_API b200norm_status b200norm_testing_force(int row_mode, int group_route);
 
+/* Force the row schedule of SkipSimplifiedLayerNormalization and
+ * GatedRMSNorm calls on the calling thread to one row per cluster of `csize`
+ * CTAs, each thread holding `nv` vectors: csize in {1, 2, 4, 8, 16}, nv in
+ * {1, 2, 4, 8}; (0, 0) restores the automatic choice.  A later call whose
+ * row would need more than 512 threads per CTA under the forced split
+ * returns B200NORM_ERR_UNSUPPORTED; a cluster the device cannot co-schedule
+ * falls back to the walking schedule. */
+B200NORM_API b200norm_status b200norm_testing_force_split(int csize, int nv);
+
+/* Switch programmatic dependent launch off (0) or on (1, the default) for
+ * every later launch of the library, on all threads.  With it on, a kernel
+ * may be scheduled while the preceding grid on its stream drains and waits
+ * for that grid before touching memory; results are identical either way. */
+B200NORM_API b200norm_status b200norm_testing_set_pdl(int on);
+
 /* Schedule the automatic planner picks, without launching anything.
  * Rows (SSLN / GatedRMSNorm): out = {mode, ve, tpr, nv, rpg, block, csize, grid}.
  * SkipGroupNorm: out = {route, ve, nv, block, csize, grid, ctas_per_item,

@@ -4,6 +4,7 @@
 // anything, picks a schedule from the shape, element type and pointer
 // alignment (the GB300 counterpart of the pages' per-call choice among
 // implementation variants), and launches on the caller's stream.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -20,6 +21,8 @@ namespace {
 thread_local std::string g_error;
 thread_local int g_force_row_mode = 0;
 thread_local int g_force_group_route = 0;
+thread_local int g_force_csize = 0;  // forced CTA / cluster row split (0: automatic)
+thread_local int g_force_nv = 0;
 
 b200norm_status fail(b200norm_status st, const char* fmt, ...) {
   char buf[512];
@@ -82,6 +85,24 @@ b200norm_status check_eps(float eps) {
 
 constexpr int64_t kMaxGrid = 0x7fffffffLL;
 
+// The forced CTA / cluster split of b200norm_testing_force_split.
+b200norm_status forced_split(int64_t rows, int64_t n, RowPlan* p) {
+  const int64_t nvec = n / p->ve;
+  const int64_t per = static_cast<int64_t>(g_force_nv) * g_force_csize;
+  const int64_t block = ((nvec + per - 1) / per + 31) / 32 * 32;
+  if (block > 512)
+    return fail(B200NORM_ERR_UNSUPPORTED, "forced split needs %lld threads per CTA (max 512)",
+                static_cast<long long>(block));
+  p->mode = 1;
+  p->nv = g_force_nv;
+  p->rpg = 1;
+  p->csize = g_force_csize;
+  p->block = static_cast<int>(block);
+  p->tpr = p->block * p->csize;
+  p->grid = rows * p->csize;
+  return B200NORM_OK;
+}
+
 RowPlan forced_walk(int64_t rows, RowPlan p) {
   p.mode = 2;
   p.block = p.tpr = 512;
@@ -123,6 +144,8 @@ b200norm_status skip_rms_impl(const void* input, const void* skip, const void* g
   for (const void* p : ptrs)
     if (p && !aligned(p, 16)) vec = false;
   RowPlan plan = plan_rows(rows, hidden, to_dtype(T), vec);
+  if (g_force_csize)
+    if (b200norm_status st = forced_split(rows, hidden, &plan)) return st;
   if (g_force_row_mode == 2) plan = forced_walk(rows, plan);
   if (plan.grid > kMaxGrid) return fail(B200NORM_ERR_UNSUPPORTED, "too many rows for one launch");
   SkipRmsCall c{input, skip, gamma, bias, output, sum, mean, inv_std, rows, hidden, to_dtype(T),
@@ -148,6 +171,18 @@ int classify_skip(int rank, const int64_t* d, int64_t N, int64_t C, int64_t H, i
 }
 
 }  // namespace
+
+namespace b200norm {
+
+namespace {
+std::atomic<bool> g_pdl{true};
+}
+
+bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed); }
+
+void set_pdl_enabled(bool on) { g_pdl.store(on, std::memory_order_relaxed); }
+
+}  // namespace b200norm
 
 void b200norm::set_error_message(const char* msg) { g_error = msg; }
 
@@ -216,6 +251,8 @@ b200norm_status b200norm_gated_rms(const void* x, const void* gate, const void* 
   for (const void* p : ptrs)
     if (!aligned(p, 16)) vec = false;
   RowPlan plan = plan_rows(rows, C, to_dtype(T), vec);
+  if (g_force_csize)
+    if (b200norm_status st = forced_split(rows, C, &plan)) return st;
   if (g_force_row_mode == 2) plan = forced_walk(rows, plan);
   if (plan.grid > kMaxGrid) return fail(B200NORM_ERR_UNSUPPORTED, "too many rows for one launch");
   GatedCall c{x, gate, scale, y, rows, C, to_dtype(T), epsilon};
@@ -340,6 +377,24 @@ b200norm_status b200norm_testing_force(int row_mode, int group_route) {
     return fail(B200NORM_ERR_INVALID_ARGUMENT, "row_mode in {0, 2}, group_route in {0, 3}");
   g_force_row_mode = row_mode;
   g_force_group_route = group_route;
+  return ok();
+}
+
+b200norm_status b200norm_testing_force_split(int csize, int nv) {
+  const bool off = csize == 0 && nv == 0;
+  const bool pow2_c = csize == 1 || csize == 2 || csize == 4 || csize == 8 || csize == 16;
+  const bool pow2_v = nv == 1 || nv == 2 || nv == 4 || nv == 8;
+  if (!off && !(pow2_c && pow2_v))
+    return fail(B200NORM_ERR_INVALID_ARGUMENT,
+                "csize in {1, 2, 4, 8, 16} and nv in {1, 2, 4, 8}, or both 0");
+  g_force_csize = csize;
+  g_force_nv = nv;
+  return ok();
+}
+
+b200norm_status b200norm_testing_set_pdl(int on) {
+  if (on != 0 && on != 1) return fail(B200NORM_ERR_INVALID_ARGUMENT, "on must be 0 or 1");
+  set_pdl_enabled(on != 0);
   return ok();
 }
 

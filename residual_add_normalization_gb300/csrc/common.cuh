@@ -253,6 +253,21 @@ __device__ __forceinline__ Moments merge(Moments a, Moments b) {
 // ---------------------------------------------------------------------------
 // Bounded grid barrier (cooperative launches only: every CTA is resident).
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel starts with pdl_wait(): when it
+// was launched with programmatic stream serialization it may have been
+// scheduled before the preceding grid on the stream finished, and the wait
+// holds it (before any global load or store) until that grid has completed
+// and its writes are visible.  Without that launch attribute the wait returns
+// at once.  pdl_trigger() lets the next grid on the stream be scheduled once
+// every CTA of this one has started (or exited); it does not release that
+// grid's own pdl_wait() early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Control block at the start of a SkipGroupNorm workspace.
 struct Control {
   unsigned int bar_count;  // CTAs arrived at the current barrier (0 between barriers)

@@ -120,6 +120,8 @@ constexpr int kNchwUnroll = 4;
 template <typename T, typename M, int VE>
 __global__ void __launch_bounds__(kNchwThreads, 4)
 sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
+  pdl_wait();
+  pdl_trigger();
   using P = Pack<T, VE>;
   extern __shared__ float4 smem4[];
   P* sb = reinterpret_cast<P*>(smem4);
@@ -213,6 +215,8 @@ constexpr int kCoopMergeChunk = 4;
 template <typename T, typename M, int VE, int NV>
 __global__ void __launch_bounds__(kCoopMaxThreads, 1)
 sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float4 smem4[];
   float* smem = reinterpret_cast<float*>(smem4);
   float* s_K = smem + k_offset;
@@ -426,6 +430,8 @@ __device__ __forceinline__ void smem_merge(float* mn, float* mm, float* m2, int 
 template <typename T, typename M, bool CL>
 __global__ void __launch_bounds__(kTwoPhaseThreads)
 sgn_partials(const SgnArgs<T, M> a, int chunks) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float mn[kTwoPhaseThreads], mm[kTwoPhaseThreads], m2s[kTwoPhaseThreads];
   const int64_t inst = blockIdx.x / chunks;
   const int q = blockIdx.x % chunks;
@@ -475,6 +481,8 @@ sgn_partials(const SgnArgs<T, M> a, int chunks) {
 template <typename T, typename M, bool CL>
 __global__ void __launch_bounds__(kTwoPhaseThreads)
 sgn_normalize(const SgnArgs<T, M> a, int chunks) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float mn[kTwoPhaseThreads], mm[kTwoPhaseThreads], m2s[kTwoPhaseThreads];
   __shared__ float s_mean, s_rstd;
   const int64_t inst = blockIdx.x / chunks;
@@ -827,25 +835,28 @@ static cudaError_t launch_group_typed(const SkipGroupCall& c, const GroupPlan& p
   cfg.blockDim = dim3(p.block);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
 
   if (p.route == 1) {
     void* fn = pick_resident<T, M>(p.ve);
     if (!fn) return cudaErrorInvalidConfiguration;
+    unsigned nattr = 0;
     if (p.csize > 1) {
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = p.csize;
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
+      nattr = 1;
     }
+    cfg.attrs = attr;
+    cfg.numAttrs = add_pdl_attr(attr, nattr);
     int span = p.nv;
     FastDiv vpc = make_fastdiv(static_cast<unsigned>(a.HW / p.ve));
     void* args[] = {&a, &span, &vpc};
     return cudaLaunchKernelExC(&cfg, fn, args);
   }
   if (p.route == 2) {
+    // A cooperative launch keeps plain stream order (no early scheduling).
     void* fn = pick_coop<T, M>(p.ve, p.nv);
     if (!fn) return cudaErrorInvalidConfiguration;
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -859,15 +870,17 @@ static cudaError_t launch_group_typed(const SkipGroupCall& c, const GroupPlan& p
     return cudaLaunchKernelExC(&cfg, fn, args);
   }
   // route 3
-  const int chunks = p.chunks;
-  if (c.channels_last) {
-    sgn_partials<T, M, true><<<static_cast<unsigned>(p.grid), p.block, 0, stream>>>(a, chunks);
-    sgn_normalize<T, M, true><<<static_cast<unsigned>(p.grid), p.block, 0, stream>>>(a, chunks);
-  } else {
-    sgn_partials<T, M, false><<<static_cast<unsigned>(p.grid), p.block, 0, stream>>>(a, chunks);
-    sgn_normalize<T, M, false><<<static_cast<unsigned>(p.grid), p.block, 0, stream>>>(a, chunks);
-  }
-  return cudaGetLastError();
+  int chunks = p.chunks;
+  cfg.attrs = attr;
+  cfg.numAttrs = add_pdl_attr(attr, 0);
+  void* args[] = {&a, &chunks};
+  void* first = c.channels_last ? reinterpret_cast<void*>(sgn_partials<T, M, true>)
+                                : reinterpret_cast<void*>(sgn_partials<T, M, false>);
+  void* second = c.channels_last ? reinterpret_cast<void*>(sgn_normalize<T, M, true>)
+                                 : reinterpret_cast<void*>(sgn_normalize<T, M, false>);
+  cudaError_t e = cudaLaunchKernelExC(&cfg, first, args);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelExC(&cfg, second, args);
 }
 
 cudaError_t launch_group(const SkipGroupCall& c, const GroupPlan& p, cudaStream_t stream) {

@@ -85,6 +85,21 @@ struct GatedCall {
   float eps;
 };
 
+// Launches allow programmatic dependent launch (the kernel may be scheduled
+// while the preceding grid on the stream drains; it waits for that grid
+// before touching memory) unless switched off.  On by default.
+bool pdl_enabled();
+void set_pdl_enabled(bool on);
+
+// Appends the programmatic-serialization launch attribute to attrs[n] when
+// it is enabled; returns the new attribute count.
+inline unsigned add_pdl_attr(cudaLaunchAttribute* attrs, unsigned n) {
+  if (!pdl_enabled()) return n;
+  attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[n].val.programmaticStreamSerializationAllowed = 1;
+  return n + 1;
+}
+
 // Row plans depend only on the shape, element type and pointer alignment.
 RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok);
 

@@ -245,6 +245,8 @@ constexpr int lane_min_blocks(int held) {
 template <class Op, int NV, int RPG>
 __global__ void __launch_bounds__(kLaneBlock, lane_min_blocks(NV * RPG))
 rows_lane_kernel(const typename Op::Args a, int tpr, int nvec) {
+  pdl_wait();
+  pdl_trigger();
   typename Op::Wt w[NV];
   const int lane = threadIdx.x & (tpr - 1);
   const int group = threadIdx.x / tpr;
@@ -300,6 +302,8 @@ rows_lane_kernel(const typename Op::Args a, int tpr, int nvec) {
 template <class Op, int NV>
 __global__ void __launch_bounds__(kRowsMaxThreads)
 rows_cta_kernel(const typename Op::Args a, int tpr, int nvec) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[33];
   __shared__ float cl_slot;
   typename Op::In in[NV];
@@ -345,6 +349,8 @@ rows_cta_kernel(const typename Op::Args a, int tpr, int nvec) {
 template <class Op>
 __global__ void __launch_bounds__(kRowsMaxThreads)
 rows_walk_kernel(const typename Op::Args a, int nvec) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[33];
   const int64_t row = blockIdx.x;
   float acc = 0.0f;

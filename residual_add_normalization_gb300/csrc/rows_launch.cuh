@@ -67,9 +67,15 @@ RowsKernelFn<Op> pick_cta_kernel(int nv) {
 template <class Op>
 cudaError_t launch_rows_op(const typename Op::Args& a, const RowPlan& p, cudaStream_t stream) {
   const int nvec = static_cast<int>(a.n / p.ve);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  cfg.stream = stream;
   if (p.mode == 2) {
-    rows_walk_kernel<Op><<<static_cast<unsigned>(p.grid), p.block, 0, stream>>>(a, nvec);
-    return cudaGetLastError();
+    cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+    cfg.blockDim = dim3(p.block);
+    cfg.attrs = attr;
+    cfg.numAttrs = add_pdl_attr(attr, 0);
+    return cudaLaunchKernelEx(&cfg, rows_walk_kernel<Op>, a, nvec);
   }
   RowsKernelFn<Op> fn = p.mode == 0 ? pick_lane_kernel<Op>(p.nv, p.rpg) : pick_cta_kernel<Op>(p.nv);
   if (!fn) return cudaErrorInvalidConfiguration;
@@ -81,12 +87,10 @@ cudaError_t launch_rows_op(const typename Op::Args& a, const RowPlan& p, cudaStr
     if (e != cudaSuccess) return e;
     if (grid > resident) grid = resident;
   }
-  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(p.mode == 0 ? kLaneBlock : p.block);
   cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  unsigned nattr = 0;
   if (p.mode == 1 && p.csize > 1) {
     if (p.csize > 8) {
       cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -96,9 +100,10 @@ cudaError_t launch_rows_op(const typename Op::Args& a, const RowPlan& p, cudaStr
     attr[0].val.clusterDim.x = p.csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    nattr = 1;
   }
+  cfg.attrs = attr;
+  cfg.numAttrs = add_pdl_attr(attr, nattr);
   return cudaLaunchKernelEx(&cfg, fn, a, p.tpr, nvec);
 }
 

@@ -187,6 +187,12 @@ def test_force_hook_validation(lib):
     assert lib.b200norm_testing_force(1, 0) == INVALID
     assert lib.b200norm_testing_force(0, 2) == INVALID
     assert lib.b200norm_testing_force(0, 0) == OK
+    for bad in ((3, 1), (2, 3), (0, 1), (32, 1), (1, 16)):
+        assert lib.b200norm_testing_force_split(*bad) == INVALID, bad
+    assert lib.b200norm_testing_force_split(16, 8) == OK
+    assert lib.b200norm_testing_force_split(0, 0) == OK
+    assert lib.b200norm_testing_set_pdl(2) == INVALID
+    assert lib.b200norm_testing_set_pdl(1) == OK
 
 
 def test_binding_refuses_cpu_tensors():
