@@ -36,6 +36,9 @@ from residual_add_normalization_gb300 import synthetic  # noqa: E402
 METRIC = ("effective HBM GB/s and % of GB300 peak per op; rows/s (1 GPU, device-timed)")
 STEP_WORKLOADS = ["ssln_fp16_8x2048x4096", "gated_fp16_4x4096x8192_c128",
                   "sgn_nhwc_fp16_2x64x64x320", "sgn_nchw_fp32_16x1280x16x16"]
+# Decode-shaped calls, timed on their own (per-call latency, rows/s).
+DECODE_WORKLOADS = ["ssln_fp16_decode_1x4096", "ssln_fp16_decode_64x4096",
+                    "gated_fp16_decode_64x8192_c8192"]
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -123,17 +126,19 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def make_calls(torch, b2, dev):
+def make_calls(torch, b2, dev, names=None, rotate=True):
     """Device inputs, preallocated outputs and call closures per workload.
 
-    Each workload gets `nsets` independent input/output sets; the per-operator
-    timing cycles through them so that the inputs it reads (at least 129 MB of
-    traffic between two uses of a set) come from HBM, not from L2."""
+    With `rotate`, each workload gets `nsets` independent input/output sets;
+    the per-operator timing cycles through them so that the inputs it reads
+    (at least 4 x 129 MB of traffic between two uses of a set) come from HBM,
+    not from L2.  Without it there is one set (decode-shaped calls, whose
+    inputs a preceding kernel has just written)."""
     calls = []
-    for name in STEP_WORKLOADS:
+    for name in (STEP_WORKLOADS if names is None else names):
         spec, d = synthetic.workload(name)
         nsets = max(1, -(-4 * 129_000_000 // synthetic.algorithmic_bytes(name)))
-        nsets = min(nsets, 8)
+        nsets = min(nsets, 8) if rotate else 1
         fns, sets = [], []
         for _ in range(nsets):
             t = {k: (None if v is None else torch.from_numpy(v).to(dev)) for k, v in d.items()}
@@ -284,6 +289,33 @@ def run_ours(args, rank, world, dist):
         torch.cuda.synchronize()
         per_call_ms[i] = e0.elapsed_time(e1) / (op_rounds * rep)
 
+    # --- decode-shaped calls: per-call time in a graph of back-to-back calls -
+    decode = {}
+    if not args.no_decode:
+        for c in make_calls(torch, b2, dev, DECODE_WORKLOADS, rotate=False):
+            rep = 200
+            c["fn"]()
+            torch.cuda.synchronize()
+            g = capture(torch, lambda c=c, rep=rep: [c["fn"]() for _ in range(rep)], cap)
+            g.replay()
+            best = float("inf")
+            for _ in range(5):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                best = min(best, e0.elapsed_time(e1) / rep)
+            decode[c["name"]] = {
+                "us_per_call": round(best * 1e3, 3),
+                "units_per_s": round(c["units"] / (best * 1e-3), 1),
+                "units": {"skip_rms": "rows", "gated_rms": "C-spans"}[c["spec"]["op"]],
+                "GB_s": round(c["bytes"] / (best * 1e-3) / 1e9, 1),
+                "algorithmic_bytes": c["bytes"]}
+            del g
+        torch.cuda.synchronize()
+
     # --- end to end through the public API with host buffers ---------------
     e2e_steps = 0 if args.no_e2e else min(args.steps, 20)
     pinned_in = [{k: (None if v is None or not e2e_steps else torch.from_numpy(v).pin_memory())
@@ -390,6 +422,10 @@ def run_ours(args, rank, world, dist):
                       "per-operator times from graphs of repeated calls over rotating buffers",
         },
         "per_op": per_op,
+        "decode": ({"timing": "best of 5 replays of a CUDA graph of 200 back-to-back calls on "
+                              "one buffer set (inputs L2-resident, as when a preceding kernel "
+                              "has just written them); not part of `value`",
+                    **decode} if decode else None),
         "roofline": {"bound": "hbm", "kernel": dom_c["name"], "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": peak_src, "traffic": traffic,
@@ -500,6 +536,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end leg (for profiler runs)")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the decode-shaped latency measurements")
     ap.add_argument("--only", choices=STEP_WORKLOADS,
                     help="run a single workload (for profiler runs; not a bench line)")
     args = ap.parse_args()

@@ -50,9 +50,20 @@ WORKLOADS = {
         op="skip_group", seed=4, dtype=np.float32, mdtype=np.float16,
         shape=(16, 1280, 16, 16), channels_last=0, skip="full", bias=False, x_std=2.0,
         groups=32, epsilon=1e-5, activation=0, want_sum=False),
+    # Decode-shaped rows: one generated token per sequence, so a handful of
+    # rows of a 4K / 8K hidden state per call (latency-bound, rows/s).
+    "ssln_fp16_decode_1x4096": dict(
+        op="skip_rms", seed=5, dtype=np.float16, shape=(1, 4096), bias=True,
+        gamma=("normal", 1.0, 0.1), epsilon=SSLN_EPS, want_sum=True),
+    "ssln_fp16_decode_64x4096": dict(
+        op="skip_rms", seed=6, dtype=np.float16, shape=(64, 4096), bias=True,
+        gamma=("normal", 1.0, 0.1), epsilon=SSLN_EPS, want_sum=True),
+    "gated_fp16_decode_64x8192_c8192": dict(
+        op="gated_rms", seed=7, dtype=np.float16, shape=(64, 8192), C=8192,
+        epsilon=1e-5),
 }
 
-# Order the five workloads are listed in (small SSLN first).
+# Order the workloads are listed in (small SSLN first, decode shapes last).
 WORKLOAD_ORDER = list(WORKLOADS)
 
 

@@ -160,6 +160,13 @@ def test_row_planner_shapes(lib):
     # SSLN hidden 4096 fp16: CTA per row, every vector covered
     p = plan_rows(lib, 16384, 4096, F16)
     assert p["mode"] == 1 and p["csize"] == 1 and p["tpr"] * p["nv"] * p["ve"] >= 4096
+    # few rows (latency-bound): the widest CTA, fewest vectors per thread;
+    # many rows: CTAs of about 256 threads
+    assert (plan_rows(lib, 1, 4096, F16)["nv"], plan_rows(lib, 1, 4096, F16)["block"]) == (1, 512)
+    assert (plan_rows(lib, 64, 8192, F16)["nv"], plan_rows(lib, 64, 8192, F16)["block"]) == (2, 512)
+    assert (plan_rows(lib, 16384, 4096, F16)["nv"], plan_rows(lib, 16384, 4096, F16)["block"]) == (2, 256)
+    assert (plan_rows(lib, 16384, 4096, F32)["nv"], plan_rows(lib, 16384, 4096, F32)["block"]) == (4, 256)
+    assert (plan_rows(lib, 16384, 8192, F32)["nv"], plan_rows(lib, 16384, 8192, F32)["block"]) == (4, 512)
     # odd hidden: scalar path
     p = plan_rows(lib, 3, 5, F32)
     assert p["ve"] == 1 and p["tpr"] >= 5

@@ -1,4 +1,5 @@
-"""GPU parity at the five reference workloads' full sizes, in the launch
+"""GPU parity at every named workload's full size (the five reference workloads
+and the decode-shaped ones), in the launch
 configuration the benchmark times (the automatic schedule, one call per
 workload on the current stream).  The C oracle computes every output element
 here, so the comparison is element by element, not sampled."""
