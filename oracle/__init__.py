@@ -32,7 +32,16 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, F16 = 0, 1
+F32, F16, BF16 = 0, 1, 2
+
+# bfloat16 arrays are uint16 bit patterns whose dtype carries the metadata
+# {"bfloat16": True} (numpy has no bfloat16 type).
+BFLOAT16 = np.dtype(np.uint16, metadata={"bfloat16": True})
+
+
+def is_bf16(dtype) -> bool:
+    md = np.dtype(dtype).metadata
+    return bool(md and md.get("bfloat16"))
 
 # float32(1e-12): the SkipSimplifiedLayerNormalization epsilon default
 # (README, Attributes).
@@ -68,8 +77,13 @@ def _load():
             lib.orc_f32_to_f16.restype = ctypes.c_uint16
             lib.orc_f16_to_f64.argtypes = [ctypes.c_uint16]
             lib.orc_f16_to_f64.restype = ctypes.c_double
+            lib.orc_f64_to_bf16.argtypes = [ctypes.c_double]
+            lib.orc_f64_to_bf16.restype = ctypes.c_uint16
+            lib.orc_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.orc_bf16_to_f64.restype = ctypes.c_double
             for name in ("orc_f64_to_f16_array", "orc_f32_to_f16_array",
-                         "orc_f16_to_f32_array"):
+                         "orc_f16_to_f32_array", "orc_f64_to_bf16_array",
+                         "orc_f32_to_bf16_array", "orc_bf16_to_f32_array"):
                 getattr(lib, name).argtypes = [vp, vp, i64]
                 getattr(lib, name).restype = None
             lib.orc_skip_rms.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, f32]
@@ -85,11 +99,13 @@ def _load():
 
 def _code(dtype) -> int:
     dt = np.dtype(dtype)
+    if is_bf16(dt):
+        return BF16
     if dt == np.float32:
         return F32
     if dt == np.float16:
         return F16
-    raise TypeError(f"oracle supports float32 and float16 only, got {dt}")
+    raise TypeError(f"oracle supports float32, float16 and bfloat16 only, got {dt}")
 
 
 def _ptr(a):
@@ -100,7 +116,7 @@ def _c(a, dtype=None):
     if a is None:
         return None
     a = np.ascontiguousarray(a)
-    if dtype is not None and a.dtype != dtype:
+    if dtype is not None and (a.dtype != dtype or is_bf16(a.dtype) != is_bf16(dtype)):
         raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
     return a
 
@@ -128,6 +144,31 @@ def f16_to_f32(a) -> np.ndarray:
     bits = a.view(np.uint16) if a.dtype == np.float16 else a.astype(np.uint16)
     out = np.empty(bits.shape, dtype=np.float32)
     _load().orc_f16_to_f32_array(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+# --------------------------------------------------------------------------
+# bfloat16 conversions (written from the format definition in oracle.c)
+# --------------------------------------------------------------------------
+
+def f64_to_bf16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    out = np.empty(a.shape, dtype=BFLOAT16)
+    _load().orc_f64_to_bf16_array(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def f32_to_bf16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    out = np.empty(a.shape, dtype=BFLOAT16)
+    _load().orc_f32_to_bf16_array(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def bf16_to_f32(a) -> np.ndarray:
+    bits = np.ascontiguousarray(a).view(np.uint16)
+    out = np.empty(bits.shape, dtype=np.float32)
+    _load().orc_bf16_to_f32_array(_ptr(bits), _ptr(out), bits.size)
     return out
 
 

@@ -19,7 +19,11 @@
  *  - Build with -ffp-contract=off so that no fused multiply-add changes a
  *    binary32 sum; FLT_EVAL_METHOD must be 0 (x86-64 SSE, AArch64).
  *
- * Element type codes: 0 = float32, 1 = float16 (stored as uint16 bit patterns).
+ * Element type codes: 0 = float32, 1 = float16, 2 = bfloat16 (both 16-bit
+ * types stored as uint16 bit patterns).  bfloat16 is not among the pages'
+ * types; its conversion below is written from the format's definition (the
+ * upper half of a binary32: 1 sign bit, 8 exponent bits with bias 127,
+ * 7 fraction bits), rounding to nearest, ties to even.
  */
 #include <float.h>
 #include <math.h>
@@ -33,6 +37,7 @@
 
 #define ORC_F32 0
 #define ORC_F16 1
+#define ORC_BF16 2
 
 /* ------------------------------------------------------------------------ */
 /* IEEE 754 binary16 <-> binary64, from the format definition.              */
@@ -110,17 +115,95 @@ void orc_f16_to_f32_array(const uint16_t* in, float* out, int64_t n) {
 }
 
 /* ------------------------------------------------------------------------ */
+/* bfloat16 <-> binary64, from the format definition.                        */
+/* ------------------------------------------------------------------------ */
+
+/* Exact value of a bfloat16 pattern. */
+double orc_bf16_to_f64(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xff;
+    int f = h & 0x7f;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -133);            /* subnormal or zero: f * 2^-133 */
+    } else if (e == 255) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(128 + f), e - 134); /* (1.f) * 2^(e-127) */
+    }
+    return sign ? -v : v;
+}
+
+float orc_bf16_to_f32(uint16_t h) {
+    /* Every bfloat16 value is exactly representable in binary32. */
+    return (float)orc_bf16_to_f64(h);
+}
+
+/* Round a binary64 value to the nearest bfloat16, ties to even. */
+uint16_t orc_f64_to_bf16(double d) {
+    uint16_t sign = signbit(d) ? 0x8000 : 0;
+    if (isnan(d)) return (uint16_t)(sign | 0x7fc0);
+    double a = fabs(d);
+    /* Largest finite bfloat16 is (2 - 2^-7) * 2^127; the midpoint to the next
+     * step (2^128) is (2 - 2^-8) * 2^127, and a tie goes to the even
+     * neighbour, 2^128, i.e. overflow. */
+    if (a >= ldexp(2.0 - ldexp(1.0, -8), 127)) return (uint16_t)(sign | 0x7f80);
+    if (a == 0.0) return sign;
+    int E;
+    frexp(a, &E);            /* a = m * 2^E, m in [0.5, 1): unbiased exponent E-1 */
+    int unb = E - 1;
+    int q;                   /* exponent of one unit in the last place */
+    if (unb < -126) q = -133; /* subnormal range: fixed quantum 2^-133 */
+    else q = unb - 7;
+    double scaled = ldexp(a, -q);         /* exact: power-of-two scaling */
+    double fl = floor(scaled);
+    double frac = scaled - fl;            /* exact: scaled < 2^9 */
+    const int odd = fmod(fl, 2.0) != 0.0;
+    double r = fl;
+    if (frac > 0.5 || (frac == 0.5 && odd)) r = fl + 1.0;
+    uint32_t ri = (uint32_t)r;
+    uint32_t bits;
+    if (unb < -126) {
+        /* Subnormal: the pattern is the integer itself; ri == 128 carries
+         * into the smallest normal (exponent field 1, fraction 0). */
+        bits = ri;
+    } else {
+        /* Normal: ri in [128, 256]; 256 carries into the next binade. */
+        bits = ((uint32_t)(unb + 127) << 7) + (ri - 128);
+    }
+    if (bits >= 0x7f80) bits = 0x7f80;
+    return (uint16_t)(sign | bits);
+}
+
+uint16_t orc_f32_to_bf16(float f) {
+    /* binary32 -> binary64 is exact, so this is a single rounding. */
+    return orc_f64_to_bf16((double)f);
+}
+
+void orc_f64_to_bf16_array(const double* in, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f64_to_bf16(in[i]);
+}
+void orc_f32_to_bf16_array(const float* in, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_bf16(in[i]);
+}
+void orc_bf16_to_f32_array(const uint16_t* in, float* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_to_f32(in[i]);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Element access                                                            */
 /* ------------------------------------------------------------------------ */
 
 static float ld_f32(const void* p, int dtype, int64_t i) {
     if (dtype == ORC_F16) return orc_f16_to_f32(((const uint16_t*)p)[i]);
+    if (dtype == ORC_BF16) return orc_bf16_to_f32(((const uint16_t*)p)[i]);
     return ((const float*)p)[i];
 }
 
 /* Store a binary64 value at type T, rounding once to nearest-even. */
 static void st_from_f64(void* p, int dtype, int64_t i, double v) {
     if (dtype == ORC_F16) ((uint16_t*)p)[i] = orc_f64_to_f16(v);
+    else if (dtype == ORC_BF16) ((uint16_t*)p)[i] = orc_f64_to_bf16(v);
     else ((float*)p)[i] = (float)v;  /* C conversion rounds to nearest-even */
 }
 
@@ -136,6 +219,10 @@ static double residual_sum(float x, float skip, const void* bias, int dtype,
     if (dtype == ORC_F16) {
         uint16_t h = orc_f32_to_f16(t);
         s = orc_f16_to_f64(h);
+        if (s_out) ((uint16_t*)s_out)[s_index] = h;
+    } else if (dtype == ORC_BF16) {
+        uint16_t h = orc_f32_to_bf16(t);
+        s = orc_bf16_to_f64(h);
         if (s_out) ((uint16_t*)s_out)[s_index] = h;
     } else {
         s = (double)t;

@@ -25,12 +25,39 @@ deviation ``s``.
                        N(0,2), full skip N(0,1), no bias, gamma/beta fp16
                        N(1,0.1)/N(0,0.1), groups 32, eps 1e-5, no activation,
                        no S; seed 4.
+  ssln_fp16_decode_1x4096, ssln_fp16_decode_64x4096  decode-shaped
+                       SkipSimplifiedLayerNormalization fp16 (1 or 64 rows of
+                       4096), distributions as ssln_fp16_8x2048x4096; seeds 5, 6.
+  gated_fp16_decode_64x8192_c8192  decode-shaped GatedRMSNorm fp16, X/gate
+                       (64, 8192) N(0,1), C = 8192; seed 7.
+
+bfloat16 host arrays are uint16 bit patterns whose dtype is ``BFLOAT16`` (a
+uint16 dtype carrying the metadata {"bfloat16": True}); values are drawn in
+float32 and converted with torch's round-to-nearest-even conversion.
 """
 from __future__ import annotations
 
 import numpy as np
 
 SSLN_EPS = 9.999999960041972e-13  # float32(1e-12)
+
+BFLOAT16 = np.dtype(np.uint16, metadata={"bfloat16": True})
+
+
+def is_bf16(dtype) -> bool:
+    md = np.dtype(dtype).metadata
+    return bool(md and md.get("bfloat16"))
+
+
+def to_bfloat16(a) -> np.ndarray:
+    """float32 values -> BFLOAT16 bit patterns (torch's conversion)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).astype(BFLOAT16)
+
+
+def _cast(z, dtype):
+    return to_bfloat16(z) if is_bf16(dtype) else z.astype(dtype, copy=False)
 
 WORKLOADS = {
     "ssln_fp32_64x768": dict(
@@ -73,11 +100,12 @@ def _normal(rng, shape, mean, std, dtype):
         z *= np.float32(std)
     if mean != 0.0:
         z += np.float32(mean)
-    return z.astype(dtype, copy=False)
+    return _cast(z, dtype)
 
 
 def _uniform(rng, shape, lo, hi, dtype):
-    return rng.uniform(lo, hi, size=shape).astype(dtype)
+    z = rng.uniform(lo, hi, size=shape)
+    return to_bfloat16(z.astype(np.float32)) if is_bf16(dtype) else z.astype(dtype)
 
 
 def _draw(rng, spec, shape, dtype):

@@ -15,7 +15,8 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "oracle.c")
 PIN_TESTS = ["tests/test_oracle_half.py", "tests/test_oracle_ssln.py",
-             "tests/test_oracle_gated.py", "tests/test_oracle_sgn.py"]
+             "tests/test_oracle_gated.py", "tests/test_oracle_sgn.py",
+             "tests/test_oracle_bf16.py"]
 
 MUTANTS = {
     "bias_sign": ("t = t + ld_f32(bias, dtype, bias_index);",
@@ -51,6 +52,19 @@ MUTANTS = {
                        "if (frac >= 0.5) r = fl + 1.0;"),
     "half_subnormal_quantum": ("if (unb < -14) q = -24;", "if (unb < -15) q = -24;"),
     "half_overflow_threshold": ("if (a >= 65520.0)", "if (a >= 65504.0)"),
+    "bf16_ties_away": ("if (frac > 0.5 || (frac == 0.5 && odd)) r = fl + 1.0;",
+                       "if (frac >= 0.5) r = fl + 1.0;"),
+    "bf16_truncates": ("if (frac > 0.5 || (frac == 0.5 && odd)) r = fl + 1.0;",
+                       "(void)odd;"),
+    "bf16_subnormal_quantum": ("if (unb < -126) q = -133;", "if (unb < -127) q = -133;"),
+    "bf16_overflow_threshold": ("ldexp(2.0 - ldexp(1.0, -8), 127)",
+                                "ldexp(2.0 - ldexp(1.0, -7), 127)"),
+    "bf16_decode_bias": ("v = ldexp((double)(128 + f), e - 134);",
+                         "v = ldexp((double)(128 + f), e - 133);"),
+    "bf16_sum_not_rounded_before_stats": ("        s = orc_bf16_to_f64(h);\n",
+                                          "        s = (double)t;\n"),
+    "bf16_read_as_half": ("if (dtype == ORC_BF16) return orc_bf16_to_f32(((const uint16_t*)p)[i]);",
+                          "if (dtype == ORC_BF16) return orc_f16_to_f32(((const uint16_t*)p)[i]);"),
 }
 
 
