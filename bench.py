@@ -39,6 +39,9 @@ STEP_WORKLOADS = ["ssln_fp16_8x2048x4096", "gated_fp16_4x4096x8192_c128",
 # Decode-shaped calls, timed on their own (per-call latency, rows/s).
 DECODE_WORKLOADS = ["ssln_fp16_decode_1x4096", "ssln_fp16_decode_64x4096",
                     "gated_fp16_decode_64x8192_c8192"]
+# bfloat16 variants of the large workloads, timed like the step workloads.
+BF16_WORKLOADS = ["ssln_bf16_8x2048x4096", "gated_bf16_4x4096x8192_c128",
+                  "sgn_nhwc_bf16_2x64x64x320", "sgn_nchw_bf16_16x1280x16x16"]
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -126,6 +129,13 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+def host_tensor(torch, a):
+    """A CPU tensor over a host array (bfloat16 arrays are uint16 patterns)."""
+    if synthetic.is_bf16(a.dtype):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(a)
+
+
 def make_calls(torch, b2, dev, names=None, rotate=True):
     """Device inputs, preallocated outputs and call closures per workload.
 
@@ -141,7 +151,7 @@ def make_calls(torch, b2, dev, names=None, rotate=True):
         nsets = min(nsets, 8) if rotate else 1
         fns, sets = [], []
         for _ in range(nsets):
-            t = {k: (None if v is None else torch.from_numpy(v).to(dev)) for k, v in d.items()}
+            t = {k: (None if v is None else host_tensor(torch, v).to(dev)) for k, v in d.items()}
             if spec["op"] == "skip_rms":
                 y, s = torch.empty_like(t["input"]), torch.empty_like(t["input"])
                 def fn(t=t, y=y, s=s, spec=spec):
@@ -181,6 +191,48 @@ def capture(torch, fn, stream):
     with torch.cuda.graph(g, stream=stream):
         fn()
     return g
+
+
+def op_graphs_of(torch, calls, stream):
+    """One graph per workload: 4 x nsets calls cycling through its sets."""
+    graphs, reps = [], []
+    for c in calls:
+        rep = 4 * len(c["fns"])
+        def many(c=c, rep=rep):
+            for r in range(rep):
+                c["fns"][r % len(c["fns"])]()
+        graphs.append(capture(torch, many, stream))
+        reps.append(rep)
+    return graphs, reps
+
+
+def time_op_graphs(torch, graphs, reps, rounds, stream):
+    """Milliseconds per call of each workload: CUDA events around `rounds`
+    replays of its graph (after one untimed replay)."""
+    out = np.zeros(len(graphs))
+    for i, (g, rep) in enumerate(zip(graphs, reps)):
+        g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(rounds):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[i] = e0.elapsed_time(e1) / (rounds * rep)
+    return out
+
+
+def op_entry(c, ms):
+    peak, _ = peak_hbm()
+    gbs = c["bytes"] / (ms * 1e-3) / 1e9
+    return {"us_per_call": round(ms * 1e3, 3), "GB_s": round(gbs, 1),
+            "frac_of_measured_peak": round(gbs / peak, 4),
+            "frac_of_8TBs_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+            "units_per_s": round(c["units"] / (ms * 1e-3), 1),
+            "units": {"skip_rms": "rows", "gated_rms": "C-spans",
+                      "skip_group": "group instances"}[c["spec"]["op"]],
+            "algorithmic_bytes": c["bytes"]}
 
 
 def launches_per_call(b2, spec):
@@ -231,14 +283,7 @@ def run_ours(args, rank, world, dist):
         step()  # an eager pass on the capture stream (library caches warm)
     torch.cuda.synchronize()
     step_graph = capture(torch, step, cap)
-    op_graphs, reps = [], []
-    for c in calls:
-        rep = 4 * len(c["fns"])
-        def many(c=c, rep=rep):
-            for r in range(rep):
-                c["fns"][r % len(c["fns"])]()
-        op_graphs.append(capture(torch, many, cap))
-        reps.append(rep)
+    op_graphs, reps = op_graphs_of(torch, calls, cap)
     torch.cuda.synchronize()
     for _ in range(3):
         step_graph.replay()
@@ -277,17 +322,22 @@ def run_ours(args, rank, world, dist):
 
     # --- per-operator launch durations (events around each operator graph) --
     op_rounds = max(3, min(50, args.steps // 20))
-    per_call_ms = np.zeros(len(calls))
-    for i, (g, rep) in enumerate(zip(op_graphs, reps)):
-        g.replay()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(op_rounds):
-            g.replay()
-        e1.record(stream)
+    per_call_ms = time_op_graphs(torch, op_graphs, reps, op_rounds, stream)
+    del op_graphs
+
+    # --- bfloat16 variants of the large workloads, timed the same way -------
+    bf16_ops = {}
+    if not args.no_bf16:
+        bcalls = make_calls(torch, b2, dev, BF16_WORKLOADS)
+        for c in bcalls:
+            for f in c["fns"]:
+                f()
         torch.cuda.synchronize()
-        per_call_ms[i] = e0.elapsed_time(e1) / (op_rounds * rep)
+        graphs, breps = op_graphs_of(torch, bcalls, cap)
+        bms = time_op_graphs(torch, graphs, breps, op_rounds, stream)
+        bf16_ops = {c["name"]: op_entry(c, ms) for c, ms in zip(bcalls, bms)}
+        del graphs, bcalls
+        torch.cuda.synchronize()
 
     # --- decode-shaped calls: per-call time in a graph of back-to-back calls -
     decode = {}
@@ -318,7 +368,7 @@ def run_ours(args, rank, world, dist):
 
     # --- end to end through the public API with host buffers ---------------
     e2e_steps = 0 if args.no_e2e else min(args.steps, 20)
-    pinned_in = [{k: (None if v is None or not e2e_steps else torch.from_numpy(v).pin_memory())
+    pinned_in = [{k: (None if v is None or not e2e_steps else host_tensor(torch, v).pin_memory())
                   for k, v in c["host"].items()} for c in calls]
     pinned_out = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in c["outs"]]
                   if e2e_steps else [] for c in calls]
@@ -390,17 +440,7 @@ def run_ours(args, rank, world, dist):
     ms_per_step = total_ms / args.steps
     value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
     peak, peak_src = peak_hbm()
-    per_op = {}
-    for c, ms in zip(calls, per_call_ms):
-        gbs = c["bytes"] / (ms * 1e-3) / 1e9
-        per_op[c["name"]] = {
-            "us_per_call": round(ms * 1e3, 3), "GB_s": round(gbs, 1),
-            "frac_of_measured_peak": round(gbs / peak, 4),
-            "frac_of_8TBs_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
-            "units_per_s": round(c["units"] / (ms * 1e-3), 1),
-            "units": {"skip_rms": "rows", "gated_rms": "C-spans",
-                      "skip_group": "group instances"}[c["spec"]["op"]],
-            "algorithmic_bytes": c["bytes"]}
+    per_op = {c["name"]: op_entry(c, ms) for c, ms in zip(calls, per_call_ms)}
     dom = int(np.argmax(per_call_ms))
     dom_c = calls[dom]
     achieved = dom_c["bytes"] / (per_call_ms[dom] * 1e-3) / 1e9
@@ -422,6 +462,8 @@ def run_ours(args, rank, world, dist):
                       "per-operator times from graphs of repeated calls over rotating buffers",
         },
         "per_op": per_op,
+        "per_op_bf16": ({"timing": "as per_op; bfloat16 storage, same shapes; not part of "
+                                   "`value`", **bf16_ops} if bf16_ops else None),
         "decode": ({"timing": "best of 5 replays of a CUDA graph of 200 back-to-back calls on "
                               "one buffer set (inputs L2-resident, as when a preceding kernel "
                               "has just written them); not part of `value`",
@@ -536,13 +578,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end leg (for profiler runs)")
+    ap.add_argument("--no-bf16", action="store_true",
+                    help="skip the bfloat16 per-operator measurements")
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the decode-shaped latency measurements")
-    ap.add_argument("--only", choices=STEP_WORKLOADS,
+    ap.add_argument("--only", choices=STEP_WORKLOADS + BF16_WORKLOADS + DECODE_WORKLOADS,
                     help="run a single workload (for profiler runs; not a bench line)")
     args = ap.parse_args()
     if args.only:
         STEP_WORKLOADS[:] = [args.only]
+        args.no_bf16 = args.no_decode = True
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))

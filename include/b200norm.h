@@ -15,10 +15,15 @@
  *   - Pointers need only be aligned to their element size.  16-byte aligned
  *     pointers (with spans that are whole 16-byte vectors) take the vector
  *     path; anything else takes a scalar path with identical results.
- *   - Element types: B200NORM_F32 (IEEE binary32) or B200NORM_F16 (IEEE
- *     binary16).  bfloat16 is not supported (GatedRMSNorm README,
- *     Description; the type constraints of all three pages list float32 and
- *     float16 only).
+ *   - Element types: B200NORM_F32 (IEEE binary32), B200NORM_F16 (IEEE
+ *     binary16) and B200NORM_BF16 (bfloat16: the upper half of a binary32).
+ *     The pages' type constraints list float32 and float16 only, and the
+ *     GatedRMSNorm README, Description, says bfloat16 is not implemented
+ *     there; this library adds it as a storage type with the same arithmetic
+ *     (binary32 compute, one rounding to nearest-even at each store).  For
+ *     SkipGroupNorm the gamma/beta type M is B200NORM_F32 or T itself, and
+ *     also B200NORM_F16 when T is B200NORM_F32; other pairs return
+ *     B200NORM_ERR_UNSUPPORTED.
  *   - Rounding: the residual sum S is formed in binary32 as
  *     (x + skip) + bias -- no add at all when bias is NULL -- and rounded once
  *     to nearest-even at the tensor type; statistics are taken over that
@@ -57,7 +62,8 @@ typedef struct CUstream_st* b200norm_stream_t;
 
 typedef enum {
     B200NORM_F32 = 0,
-    B200NORM_F16 = 1
+    B200NORM_F16 = 1,
+    B200NORM_BF16 = 2
 } b200norm_dtype;
 
 typedef enum {
@@ -162,7 +168,8 @@ B200NORM_API b200norm_status b200norm_gated_rms(const void* x, const void* gate,
  *             A (N, 1, 1, C) skip when H == W == 1 is an exact match and takes
  *             the full route (same offsets, same results).
  *   bias      T, (C), or NULL.
- *   gamma, beta  M, (C).  M is independent of T.
+ *   gamma, beta  M, (C).  M is B200NORM_F32 or T, or B200NORM_F16 when T is
+ *             B200NORM_F32.
  *   s         receives S when not NULL.
  *   groups    > 0 and must divide C.
  *   activation  0 (none) or 1 (SiLU); required.

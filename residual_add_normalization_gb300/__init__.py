@@ -35,7 +35,7 @@ _LIB_PATH = os.path.join(_HERE, "libb200norm.so")
 _lock = threading.Lock()
 _lib = None
 
-_DTYPES = {torch.float32: 0, torch.float16: 1}
+_DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 
 class B200NormError(RuntimeError):
@@ -119,7 +119,8 @@ def _cuda(name, t, device=None, dtype=None):
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
     if t.dtype not in _DTYPES:
-        raise TypeError(f"{name}: only float32 and float16 are supported (got {t.dtype})")
+        raise TypeError(f"{name}: only float32, float16 and bfloat16 are supported "
+                        f"(got {t.dtype})")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t

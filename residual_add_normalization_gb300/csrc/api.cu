@@ -43,9 +43,19 @@ b200norm_status cuda_fail(cudaError_t e, const char* what) {
   return fail(B200NORM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-bool dtype_ok(b200norm_dtype t) { return t == B200NORM_F32 || t == B200NORM_F16; }
+bool dtype_ok(b200norm_dtype t) {
+  return t == B200NORM_F32 || t == B200NORM_F16 || t == B200NORM_BF16;
+}
 
-DType to_dtype(b200norm_dtype t) { return t == B200NORM_F32 ? DType::F32 : DType::F16; }
+DType to_dtype(b200norm_dtype t) {
+  return t == B200NORM_F32 ? DType::F32 : t == B200NORM_F16 ? DType::F16 : DType::BF16;
+}
+
+// SkipGroupNorm (T, M) pairs with kernels: M = float32 or T, and float16
+// gamma/beta under float32 X.
+bool group_types_ok(b200norm_dtype t, b200norm_dtype m) {
+  return dtype_ok(t) && (m == B200NORM_F32 || m == t || (t == B200NORM_F32 && m == B200NORM_F16));
+}
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -274,7 +284,7 @@ b200norm_status b200norm_skip_group(const void* x, const void* skip, int skip_ra
                                     float epsilon, int activation, int channels_last,
                                     void* workspace, size_t workspace_bytes,
                                     b200norm_stream_t stream) {
-  if (!dtype_ok(T) || !dtype_ok(M))
+  if (!group_types_ok(T, M))
     return fail(B200NORM_ERR_UNSUPPORTED, "element types T=%d M=%d not supported", T, M);
   if (N < 0 || C <= 0 || H < 0 || W < 0)
     return fail(B200NORM_ERR_INVALID_ARGUMENT, "need N >= 0, C > 0, H >= 0, W >= 0");
@@ -412,7 +422,7 @@ b200norm_status b200norm_testing_plan_rows(int64_t rows, int64_t n, b200norm_dty
 b200norm_status b200norm_testing_plan_group(int64_t N, int64_t C, int64_t H, int64_t W, int groups,
                                             b200norm_dtype T, b200norm_dtype M, int channels_last,
                                             int aligned16, int64_t out[8]) {
-  if (!dtype_ok(T) || !dtype_ok(M) || N <= 0 || C <= 0 || H <= 0 || W <= 0 || groups <= 0 ||
+  if (!group_types_ok(T, M) || N <= 0 || C <= 0 || H <= 0 || W <= 0 || groups <= 0 ||
       C % groups != 0 || !out)
     return fail(B200NORM_ERR_INVALID_ARGUMENT, "bad plan query");
   SkipGroupCall c{};

@@ -6,6 +6,7 @@
 // grid-wide barrier for cooperative launches.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -19,12 +20,42 @@ namespace b200norm {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
+// A bfloat16 is the upper half of a binary32: widening is a 16-bit shift.
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) {
+  return __uint_as_float(static_cast<unsigned>(__bfloat16_as_ushort(v)) << 16);
+}
 
 template <typename T> __device__ __forceinline__ T from_f32(float v);
 template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <> __device__ __forceinline__ __half from_f32<__half>(float v) {
   return __float2half_rn(v);  // round to nearest-even, subnormals kept
 }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);  // round to nearest-even, subnormals kept
+}
+
+// The 16-bit types convert two elements at a time (one instruction each way).
+template <typename T> struct Pair2 { static constexpr bool kPacked = false; };
+template <> struct Pair2<__half> {
+  static constexpr bool kPacked = true;
+  using type = __half2;
+  __device__ __forceinline__ static float2 widen(type v) { return __half22float2(v); }
+  __device__ __forceinline__ static type narrow(float a, float b) {
+    return __floats2half2_rn(a, b);
+  }
+};
+template <> struct Pair2<__nv_bfloat16> {
+  static constexpr bool kPacked = true;
+  using type = __nv_bfloat162;
+  __device__ __forceinline__ static float2 widen(type v) {
+    unsigned w;
+    memcpy(&w, &v, sizeof(w));
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+  __device__ __forceinline__ static type narrow(float a, float b) {
+    return __floats2bfloat162_rn(a, b);
+  }
+};
 
 // A pack of N elements of T moved as one access of sizeof(T) * N bytes.
 template <typename T, int N>
@@ -70,10 +101,11 @@ __device__ __forceinline__ void st_stream(T* p, const Pack<T, N>& v) {
 // Widen a pack to binary32 (pairs of halves convert with one instruction).
 template <typename T, int N>
 __device__ __forceinline__ void unpack(const Pack<T, N>& p, float (&f)[N]) {
-  if constexpr (std::is_same<T, __half>::value && N % 2 == 0) {
+  if constexpr (Pair2<T>::kPacked && N % 2 == 0) {
+    using P2 = Pair2<T>;
 #pragma unroll
     for (int i = 0; i < N / 2; ++i) {
-      const float2 t = __half22float2(reinterpret_cast<const __half2*>(p.v)[i]);
+      const float2 t = P2::widen(reinterpret_cast<const typename P2::type*>(p.v)[i]);
       f[2 * i] = t.x;
       f[2 * i + 1] = t.y;
     }
@@ -87,10 +119,11 @@ __device__ __forceinline__ void unpack(const Pack<T, N>& p, float (&f)[N]) {
 template <typename T, int N>
 __device__ __forceinline__ Pack<T, N> pack_from(const float (&f)[N]) {
   Pack<T, N> p;
-  if constexpr (std::is_same<T, __half>::value && N % 2 == 0) {
+  if constexpr (Pair2<T>::kPacked && N % 2 == 0) {
+    using P2 = Pair2<T>;
 #pragma unroll
     for (int i = 0; i < N / 2; ++i)
-      reinterpret_cast<__half2*>(p.v)[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+      reinterpret_cast<typename P2::type*>(p.v)[i] = P2::narrow(f[2 * i], f[2 * i + 1]);
   } else {
 #pragma unroll
     for (int i = 0; i < N; ++i) p.v[i] = from_f32<T>(f[i]);
@@ -99,19 +132,19 @@ __device__ __forceinline__ Pack<T, N> pack_from(const float (&f)[N]) {
 }
 
 // Element pair (2i, 2i+1) of a pack as binary32, and the reverse (each value
-// rounded to nearest-even).  For halves one instruction converts both.
+// rounded to nearest-even).  For 16-bit types one instruction converts both.
 template <typename T, int N>
 __device__ __forceinline__ float2 get2(const Pack<T, N>& p, int i) {
-  if constexpr (std::is_same<T, __half>::value)
-    return __half22float2(reinterpret_cast<const __half2*>(p.v)[i]);
+  if constexpr (Pair2<T>::kPacked)
+    return Pair2<T>::widen(reinterpret_cast<const typename Pair2<T>::type*>(p.v)[i]);
   else
     return make_float2(to_f32(p.v[2 * i]), to_f32(p.v[2 * i + 1]));
 }
 
 template <typename T, int N>
 __device__ __forceinline__ void set2(Pack<T, N>& p, int i, float a, float b) {
-  if constexpr (std::is_same<T, __half>::value)
-    reinterpret_cast<__half2*>(p.v)[i] = __floats2half2_rn(a, b);
+  if constexpr (Pair2<T>::kPacked)
+    reinterpret_cast<typename Pair2<T>::type*>(p.v)[i] = Pair2<T>::narrow(a, b);
   else {
     p.v[2 * i] = from_f32<T>(a);
     p.v[2 * i + 1] = from_f32<T>(b);

@@ -1,0 +1,663 @@
+// group_kernels.cuh -- SkipGroupNorm kernels (sm_103a), included by the
+// per-element-type translation units group_f32.cu, group_f16.cu and
+// group_bf16.cu, and by the planner in group_norm.cu.
+//
+// S = round_T((X + skip) + bias); Y = round_T(act((S - mean) * rstd * gamma[c] + beta[c]))
+// with mean / population variance per (batch item n, group g) over the C/groups
+// channels of g and every spatial position (com.microsoft.SkipGroupNorm README,
+// Description).  Three routes:
+//
+//   1. NCHW resident.  A group instance (n, g) is one contiguous run of
+//      cpg * H * W elements.  One CTA -- or a cluster of up to 16 CTAs for
+//      long runs -- stages its share of S in shared memory: one HBM read,
+//      exact two-pass (centred) statistics from shared memory, one write.
+//      Cluster partials are exchanged through distributed shared memory.
+//   2. NHWC cooperative.  A group's elements are strided through the tensor
+//      (cpg channels of every pixel), so statistics need every CTA that holds
+//      a piece of the batch item.  One cooperative grid: each CTA holds a
+//      slab of whole pixels in registers, takes its slab's per-group
+//      (count, mean, M2) with two passes of plain additions, publishes them,
+//      meets the other CTAs at one bounded grid barrier, merges its batch
+//      item's partials with Chan's formula and normalizes what it holds.
+//   3. Two-phase, any shape or layout.  Kernel A forms S over fixed chunks of
+//      each group instance and writes per-chunk moments; kernel B merges them
+//      and re-forms S from the inputs to normalize (the re-read is an L2 hit
+//      for anything that fits in L2).
+//
+// Every route carries the group mean as K + d: K an exact data value of the
+// group (its first residual sum), d the mean of S - K.  S - K is exact for
+// data near the mean, so (S - K) - d stays accurate in binary32 even when
+// |mean| is large against the group's spread.
+#pragma once
+
+#include <cstring>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace b200norm {
+
+template <typename T, typename M>
+struct SgnArgs {
+  const T* __restrict__ x;
+  const T* __restrict__ skip;
+  const T* __restrict__ bias;   // may be null
+  const M* __restrict__ gamma;
+  const M* __restrict__ beta;
+  T* __restrict__ y;
+  T* __restrict__ s;            // may be null
+  int64_t N;
+  int C, HW, cpg, groups;
+  int bcast;                    // skip holds one value per (n, c)
+  int act;                      // 1: SiLU after the affine transform
+  float eps;
+  Control* ctl;                 // workspace control block
+  float4* part;                 // workspace moment slots (n, mean, M2, -)
+  unsigned long long limit_ns;  // bound of every cross-CTA wait
+};
+
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr int kCoopMaxThreads = 512;
+constexpr int kTwoPhaseThreads = 256;
+constexpr int kTwoPhaseEpt = kTwoPhaseChunk / kTwoPhaseThreads;
+
+// S element at type T from binary32 x and skip, plus bias when present.
+template <typename T>
+__device__ __forceinline__ T sgn_sum(float x, float sk, const T* __restrict__ bias, int c) {
+  float t = __fadd_rn(x, sk);
+  if (bias) t = __fadd_rn(t, to_f32(bias[c]));
+  return from_f32<T>(t);
+}
+
+// ((S - K) - d) * rstd * gamma + beta, then SiLU when requested.
+__device__ __forceinline__ float sgn_out(float s, float K, float d, float rstd, float ga,
+                                         float be, int act) {
+  float z = ((s - K) - d) * rstd * ga + be;
+  if (act) z = silu_f32(z);
+  return z;
+}
+
+// Shift K of group instance (n, g): its residual sum at (channel g*cpg, pixel 0).
+template <typename T, typename M>
+__device__ __forceinline__ float sgn_shift(const SgnArgs<T, M>& a, int64_t n, int g, bool cl) {
+  const int c = g * a.cpg;
+  const int64_t off = cl ? n * a.HW * a.C + c : (n * a.C + c) * static_cast<int64_t>(a.HW);
+  const float sk = a.bcast ? to_f32(a.skip[n * a.C + c]) : to_f32(a.skip[off]);
+  return to_f32(sgn_sum<T>(to_f32(a.x[off]), sk, a.bias, c));
+}
+
+// Division by an invariant divisor as a multiply and a shift (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994):
+// for 0 <= n < 2^31, n / d = (umulhi(n, m) + n) >> l with l = ceil(log2 d) and
+// m = floor(2^32 * (2^l - d) / d) + 1.
+struct FastDiv {
+  unsigned m, l;
+};
+
+inline FastDiv make_fastdiv(unsigned d) {
+  unsigned l = 0;
+  while ((1ull << l) < d) ++l;
+  FastDiv f;
+  f.m = static_cast<unsigned>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+  f.l = l;
+  return f;
+}
+
+__device__ __forceinline__ unsigned fdiv(unsigned n, FastDiv f) {
+  return (__umulhi(n, f.m) + n) >> f.l;
+}
+
+// ---------------------------------------------------------------------------
+// Route 1: NCHW, one CTA or cluster per group instance, S staged in shared
+// memory
+// ---------------------------------------------------------------------------
+// A group instance (n, g) is the contiguous run of L = cpg * H * W elements at
+// (n*C + g*cpg) * H*W.  CTA rank r of the instance's cluster takes vectors
+// [r * span, (r + 1) * span) of it: it loads X (+ skip), forms S, keeps S in
+// shared memory (span vectors of dynamic shared memory), and takes exact
+// two-pass statistics from there; cluster partial sums meet through DSMEM.
+// VE > 1 needs H*W % VE == 0 so that a vector never straddles two channels;
+// vpc = H*W / VE vectors per channel.
+constexpr int kNchwThreads = 256;
+constexpr int kNchwUnroll = 4;
+
+template <typename T, typename M, int VE>
+__global__ void __launch_bounds__(kNchwThreads, 4)
+sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
+  pdl_wait();
+  pdl_trigger();
+  using P = Pack<T, VE>;
+  extern __shared__ float4 smem4[];
+  P* sb = reinterpret_cast<P*>(smem4);
+  __shared__ float red[33];
+  __shared__ float slot_sum, slot_m2;
+  const unsigned csize = cluster_size();
+  const unsigned rank = csize > 1 ? cluster_rank() : 0u;
+  const int64_t inst = blockIdx.x / csize;
+  const int64_t n = inst / a.groups;
+  const int g = static_cast<int>(inst % a.groups);
+  const int L = a.cpg * a.HW;
+  const int v0 = static_cast<int>(rank) * span;
+  const int cnt = min(span, L / VE - v0);  // may be <= 0 for trailing ranks
+  const int64_t base = (n * a.C + static_cast<int64_t>(g) * a.cpg) * a.HW + static_cast<int64_t>(v0) * VE;
+  const int cbase = g * a.cpg;
+
+  const float K = sgn_shift(a, n, g, false);
+  float sum = 0.0f;
+  for (int i0 = threadIdx.x; i0 < cnt; i0 += kNchwThreads * kNchwUnroll) {
+    P xv[kNchwUnroll], kv[kNchwUnroll];
+#pragma unroll
+    for (int u = 0; u < kNchwUnroll; ++u) {
+      const int i = i0 + u * kNchwThreads;
+      if (i < cnt) {
+        xv[u] = ld_stream<T, VE>(a.x + base + static_cast<int64_t>(i) * VE);
+        if (!a.bcast) kv[u] = ld_stream<T, VE>(a.skip + base + static_cast<int64_t>(i) * VE);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kNchwUnroll; ++u) {
+      const int i = i0 + u * kNchwThreads;
+      if (i < cnt) {
+        const int c = cbase + static_cast<int>(fdiv(static_cast<unsigned>(v0 + i), vpc));
+        const float skb = a.bcast ? to_f32(a.skip[n * a.C + c]) : 0.0f;
+        P sv;
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          const float sk = a.bcast ? skb : to_f32(kv[u].v[e]);
+          sv.v[e] = sgn_sum<T>(to_f32(xv[u].v[e]), sk, a.bias, c);
+          sum += to_f32(sv.v[e]) - K;
+        }
+        sb[i] = sv;
+        if (a.s) st_stream<T, VE>(a.s + base + static_cast<int64_t>(i) * VE, sv);
+      }
+    }
+  }
+  float tot = cta_sum(sum, red);
+  if (csize > 1) tot = cluster_sum(tot, &slot_sum, csize);
+  const float dmean = tot / static_cast<float>(L);  // mean = K + dmean
+  float m2 = 0.0f;
+  for (int i = threadIdx.x; i < cnt; i += kNchwThreads) {
+    const P sv = sb[i];
+#pragma unroll
+    for (int e = 0; e < VE; ++e) {
+      const float d = (to_f32(sv.v[e]) - K) - dmean;
+      m2 = fmaf(d, d, m2);
+    }
+  }
+  tot = cta_sum(m2, red);
+  if (csize > 1) tot = cluster_sum(tot, &slot_m2, csize);
+  const float rstd = 1.0f / sqrtf(tot / static_cast<float>(L) + a.eps);
+  for (int i = threadIdx.x; i < cnt; i += kNchwThreads) {
+    const int c = cbase + static_cast<int>(fdiv(static_cast<unsigned>(v0 + i), vpc));
+    const float ga = to_f32(a.gamma[c]), be = to_f32(a.beta[c]);
+    const P sv = sb[i];
+    P out;
+#pragma unroll
+    for (int e = 0; e < VE; ++e)
+      out.v[e] = from_f32<T>(sgn_out(to_f32(sv.v[e]), K, dmean, rstd, ga, be, a.act));
+    st_stream<T, VE>(a.y + base + static_cast<int64_t>(i) * VE, out);
+  }
+  if (csize > 1) cluster_sync();  // peers may still read slot_m2
+}
+
+// ---------------------------------------------------------------------------
+// Route 2: NHWC, cooperative grid with one bounded grid barrier
+// ---------------------------------------------------------------------------
+// blockDim.x = CV * PL with CV = C / VE vectors per pixel: thread t covers the
+// VE channels (t % CV) * VE .. +VE of pixels p0 + t / CV + k * PL, k < NV.
+// CTA b handles batch item b / B, pixels [(b % B) * ppc, +ppc).
+// Inside a CTA the statistics are an exact two-pass over the held S (sums
+// only: per thread, per pixel lane and channel, then per group); across CTAs
+// the (count, mean, M2) partials meet with Chan's merge after one grid
+// barrier.  All moments are of S - K[g], K[g] the group's first residual sum.
+// Dynamic shared memory (floats), layout given by k_offset:
+//   passes:  acc[PL*C] | col[C] | gmean[groups]
+//   merge:   chunk moments[nchunk*groups*3] | gmean[groups] | grstd[groups]
+//   tail at k_offset, kept throughout: K[groups] | gamma[C] | beta[C]
+constexpr int kCoopMergeChunk = 4;
+
+template <typename T, typename M, int VE, int NV>
+__global__ void __launch_bounds__(kCoopMaxThreads, 1)
+sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ float4 smem4[];
+  float* smem = reinterpret_cast<float*>(smem4);
+  float* s_K = smem + k_offset;
+  const int C = a.C;
+  const int CV = C / VE;
+  const int PL = blockDim.x / CV;
+  const int tc = threadIdx.x % CV;
+  const int tp = threadIdx.x / CV;
+  const int n = blockIdx.x / B;
+  const int p0 = (blockIdx.x % B) * ppc;
+  const int p1 = min(p0 + ppc, a.HW);
+  const int64_t nbase = static_cast<int64_t>(n) * a.HW * C;
+  const int c0 = tc * VE;
+
+  // --- load and form S (S is stored after the barrier, with Y) ------------
+  Pack<T, VE> xv[NV], kv[NV], sv[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int p = p0 + tp + k * PL;
+    if (p < p1) {
+      const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+      xv[k] = ld_stream<T, VE>(a.x + off);
+      if (!a.bcast) kv[k] = ld_stream<T, VE>(a.skip + off);
+    }
+  }
+  Pack<T, VE> skb;
+  if (a.bcast) skb = ld_reuse<T, VE>(a.skip + static_cast<int64_t>(n) * C + c0);
+  // the affine weights are needed only at the end: stage them now
+  float* s_ga = s_K + a.groups;
+  float* s_be = s_ga + C;
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    s_ga[c] = to_f32(__ldg(a.gamma + c));
+    s_be[c] = to_f32(__ldg(a.beta + c));
+  }
+  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) s_K[gg] = sgn_shift(a, n, gg, true);
+  __syncthreads();
+  float Kl[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) Kl[e] = s_K[(c0 + e) / a.cpg];
+  float lsum[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) lsum[e] = 0.0f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int p = p0 + tp + k * PL;
+    if (p < p1) {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        const float sk = a.bcast ? to_f32(skb.v[e]) : to_f32(kv[k].v[e]);
+        sv[k].v[e] = sgn_sum<T>(to_f32(xv[k].v[e]), sk, a.bias, c0 + e);
+        lsum[e] += to_f32(sv[k].v[e]) - Kl[e];
+      }
+    }
+  }
+  // acc is laid out [e][tp][tc] so that the stores of a warp hit distinct banks
+  float* s_acc = smem;
+  float* s_col = smem + PL * C;
+  float* s_gm = s_col + C;
+  const float n_cta = static_cast<float>(p1 - p0) * static_cast<float>(a.cpg);
+
+  // --- pass 1: CTA-local group means of S - K ----------------------------
+#pragma unroll
+  for (int e = 0; e < VE; ++e) s_acc[(e * PL + tp) * CV + tc] = lsum[e];
+  __syncthreads();
+  for (int j = threadIdx.x; j < C; j += blockDim.x) {
+    const int e = j / CV, q0 = j % CV;
+    float t = 0.0f;
+    for (int q = 0; q < PL; ++q) t += s_acc[(e * PL + q) * CV + q0];
+    s_col[q0 * VE + e] = t;
+  }
+  __syncthreads();
+  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
+    float t = 0.0f;
+    for (int cc = 0; cc < a.cpg; ++cc) t += s_col[gg * a.cpg + cc];
+    s_gm[gg] = t / n_cta;
+  }
+  __syncthreads();
+  // --- pass 2: CTA-local sums of squared deviations ----------------------
+  float gml[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) gml[e] = s_gm[(c0 + e) / a.cpg];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) {
+    float m2 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int p = p0 + tp + k * PL;
+      if (p < p1) {
+        const float d = (to_f32(sv[k].v[e]) - Kl[e]) - gml[e];
+        m2 = fmaf(d, d, m2);
+      }
+    }
+    s_acc[(e * PL + tp) * CV + tc] = m2;
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < C; j += blockDim.x) {
+    const int e = j / CV, q0 = j % CV;
+    float t = 0.0f;
+    for (int q = 0; q < PL; ++q) t += s_acc[(e * PL + q) * CV + q0];
+    s_col[q0 * VE + e] = t;
+  }
+  __syncthreads();
+  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
+    float t = 0.0f;
+    for (int cc = 0; cc < a.cpg; ++cc) t += s_col[gg * a.cpg + cc];
+    a.part[static_cast<int64_t>(blockIdx.x) * a.groups + gg] = make_float4(n_cta, s_gm[gg], t, 0.0f);
+  }
+  __threadfence();  // partials visible GPU-wide before this CTA arrives
+  if (!grid_barrier(a.ctl, gridDim.x, a.limit_ns, 1u)) return;
+
+  // --- merge the batch item's B partials per group ------------------------
+  // chunks of kCoopMergeChunk partials: all loads of a chunk are issued
+  // before its merges, then the chunk results are merged per group
+  const int nchunk = (B + kCoopMergeChunk - 1) / kCoopMergeChunk;
+  float* s_cm = smem;                                  // nchunk * groups * 3
+  float* s_gmean = smem + nchunk * a.groups * 3;
+  float* s_grstd = s_gmean + a.groups;
+  const float4* src = a.part + static_cast<int64_t>(n) * B * a.groups;
+  for (int idx = threadIdx.x; idx < nchunk * a.groups; idx += blockDim.x) {
+    const int gg = idx % a.groups, q = idx / a.groups;
+    const int b0 = q * kCoopMergeChunk;
+    float4 u[kCoopMergeChunk];
+#pragma unroll
+    for (int j = 0; j < kCoopMergeChunk; ++j)
+      if (b0 + j < B) u[j] = __ldcg(src + static_cast<int64_t>(b0 + j) * a.groups + gg);
+    Moments m{0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int j = 0; j < kCoopMergeChunk; ++j)
+      if (b0 + j < B) m = merge(m, Moments{u[j].x, u[j].y, u[j].z});
+    s_cm[idx * 3] = m.n;
+    s_cm[idx * 3 + 1] = m.mean;
+    s_cm[idx * 3 + 2] = m.m2;
+  }
+  __syncthreads();
+  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
+    Moments m{0.0f, 0.0f, 0.0f};
+    for (int q = 0; q < nchunk; ++q) {
+      const int idx = q * a.groups + gg;
+      m = merge(m, Moments{s_cm[idx * 3], s_cm[idx * 3 + 1], s_cm[idx * 3 + 2]});
+    }
+    s_gmean[gg] = m.mean;
+    s_grstd[gg] = 1.0f / sqrtf(m.m2 / m.n + a.eps);
+  }
+  __syncthreads();
+  // --- normalize what this thread holds; store S and Y ---------------------
+  float mu[VE], rs[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) {
+    mu[e] = s_gmean[(c0 + e) / a.cpg];
+    rs[e] = s_grstd[(c0 + e) / a.cpg];
+  }
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int p = p0 + tp + k * PL;
+    if (p < p1) {
+      const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+      if (a.s) st_stream<T, VE>(a.s + off, sv[k]);
+      Pack<T, VE> out;
+#pragma unroll
+      for (int e = 0; e < VE; ++e)
+        out.v[e] = from_f32<T>(sgn_out(to_f32(sv[k].v[e]), Kl[e], mu[e], rs[e],
+                                       s_ga[c0 + e], s_be[c0 + e], a.act));
+      st_stream<T, VE>(a.y + off, out);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Route 3: two-phase, any layout
+// ---------------------------------------------------------------------------
+// Element j of group instance (n, g), j in [0, cpg*HW):
+//   NCHW: offset (n*C + g*cpg)*HW + j,                 channel g*cpg + j / HW
+//   NHWC: offset (n*HW + j / cpg)*C + g*cpg + j % cpg,  channel g*cpg + j % cpg
+template <typename T, typename M>
+__device__ __forceinline__ void sgn_locate(const SgnArgs<T, M>& a, int64_t n, int g, int64_t j,
+                                           bool cl, int64_t* off, int* c) {
+  if (cl) {
+    const int64_t p = j / a.cpg;
+    const int cc = static_cast<int>(j % a.cpg);
+    *c = g * a.cpg + cc;
+    *off = (n * a.HW + p) * a.C + *c;
+  } else {
+    *c = g * a.cpg + static_cast<int>(j / a.HW);
+    *off = (n * a.C + static_cast<int64_t>(g) * a.cpg) * a.HW + j;
+  }
+}
+
+template <typename T, typename M>
+__device__ __forceinline__ float sgn_form(const SgnArgs<T, M>& a, int64_t n, int64_t off, int c) {
+  const float x = to_f32(__ldcs(a.x + off));
+  const float sk = a.bcast ? to_f32(a.skip[n * a.C + c]) : to_f32(__ldcs(a.skip + off));
+  return to_f32(sgn_sum<T>(x, sk, a.bias, c));
+}
+
+// Merge `count` moments held in shared memory (tree, fixed order); result in [0].
+__device__ __forceinline__ void smem_merge(float* mn, float* mm, float* m2, int count) {
+  for (int stride = 1; stride < count; stride <<= 1) {
+    for (int i = threadIdx.x; i < count; i += blockDim.x) {
+      if ((i % (2 * stride)) == 0 && i + stride < count) {
+        const Moments r = merge(Moments{mn[i], mm[i], m2[i]},
+                                Moments{mn[i + stride], mm[i + stride], m2[i + stride]});
+        mn[i] = r.n;
+        mm[i] = r.mean;
+        m2[i] = r.m2;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <typename T, typename M, bool CL>
+__global__ void __launch_bounds__(kTwoPhaseThreads)
+sgn_partials(const SgnArgs<T, M> a, int chunks) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float mn[kTwoPhaseThreads], mm[kTwoPhaseThreads], m2s[kTwoPhaseThreads];
+  const int64_t inst = blockIdx.x / chunks;
+  const int q = blockIdx.x % chunks;
+  const int64_t n = inst / a.groups;
+  const int g = static_cast<int>(inst % a.groups);
+  const int64_t L = static_cast<int64_t>(a.cpg) * a.HW;
+  const int64_t j0 = static_cast<int64_t>(q) * kTwoPhaseChunk;
+  const float K = sgn_shift(a, n, g, CL);
+  float v[kTwoPhaseEpt];
+  int cnt = 0;
+  float sum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kTwoPhaseEpt; ++i) {
+    const int64_t j = j0 + threadIdx.x + static_cast<int64_t>(i) * kTwoPhaseThreads;
+    v[i] = 0.0f;
+    if (j < L) {
+      int64_t off;
+      int c;
+      sgn_locate(a, n, g, j, CL, &off, &c);
+      const float x = to_f32(__ldcs(a.x + off));
+      const float sk = a.bcast ? to_f32(a.skip[n * a.C + c]) : to_f32(__ldcs(a.skip + off));
+      const T sT = sgn_sum<T>(x, sk, a.bias, c);
+      if (a.s) a.s[off] = sT;
+      v[i] = to_f32(sT) - K;
+      sum += v[i];
+      ++cnt;
+    }
+  }
+  const float mu = cnt ? sum / static_cast<float>(cnt) : 0.0f;
+  float m2 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kTwoPhaseEpt; ++i) {
+    const int64_t j = j0 + threadIdx.x + static_cast<int64_t>(i) * kTwoPhaseThreads;
+    if (j < L) {
+      const float d = v[i] - mu;
+      m2 = fmaf(d, d, m2);
+    }
+  }
+  mn[threadIdx.x] = static_cast<float>(cnt);
+  mm[threadIdx.x] = mu;
+  m2s[threadIdx.x] = m2;
+  __syncthreads();
+  smem_merge(mn, mm, m2s, blockDim.x);
+  if (threadIdx.x == 0) a.part[blockIdx.x] = make_float4(mn[0], mm[0], m2s[0], 0.0f);
+}
+
+template <typename T, typename M, bool CL>
+__global__ void __launch_bounds__(kTwoPhaseThreads)
+sgn_normalize(const SgnArgs<T, M> a, int chunks) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float mn[kTwoPhaseThreads], mm[kTwoPhaseThreads], m2s[kTwoPhaseThreads];
+  __shared__ float s_mean, s_rstd;
+  const int64_t inst = blockIdx.x / chunks;
+  const int q = blockIdx.x % chunks;
+  const int64_t n = inst / a.groups;
+  const int g = static_cast<int>(inst % a.groups);
+  const int64_t L = static_cast<int64_t>(a.cpg) * a.HW;
+  // merge this instance's chunk moments: each thread folds a strided subset
+  // in order, then a tree over threads
+  Moments m{0.0f, 0.0f, 0.0f};
+  for (int i = threadIdx.x; i < chunks; i += blockDim.x) {
+    const float4 u = __ldcg(a.part + inst * chunks + i);
+    m = merge(m, Moments{u.x, u.y, u.z});
+  }
+  mn[threadIdx.x] = m.n;
+  mm[threadIdx.x] = m.mean;
+  m2s[threadIdx.x] = m.m2;
+  __syncthreads();
+  smem_merge(mn, mm, m2s, blockDim.x);
+  if (threadIdx.x == 0) {
+    s_mean = mm[0];
+    s_rstd = 1.0f / sqrtf(m2s[0] / mn[0] + a.eps);
+  }
+  __syncthreads();
+  const float dmean = s_mean, rstd = s_rstd;
+  const float K = sgn_shift(a, n, g, CL);
+  const int64_t j0 = static_cast<int64_t>(q) * kTwoPhaseChunk;
+#pragma unroll 4
+  for (int i = 0; i < kTwoPhaseEpt; ++i) {
+    const int64_t j = j0 + threadIdx.x + static_cast<int64_t>(i) * kTwoPhaseThreads;
+    if (j < L) {
+      int64_t off;
+      int c;
+      sgn_locate(a, n, g, j, CL, &off, &c);
+      const float sv = sgn_form(a, n, off, c);
+      a.y[off] = from_f32<T>(
+          sgn_out(sv, K, dmean, rstd, to_f32(a.gamma[c]), to_f32(a.beta[c]), a.act));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Kernel selection and typed launch (host)
+// ---------------------------------------------------------------------------
+inline size_t coop_k_offset(int PL, int C, int B, int groups) {
+  const size_t passes = static_cast<size_t>(PL) * C + C + groups;
+  const size_t nchunk = (static_cast<size_t>(B) + kCoopMergeChunk - 1) / kCoopMergeChunk;
+  const size_t merge = nchunk * groups * 3 + 2ull * groups;
+  return passes > merge ? passes : merge;
+}
+
+template <typename T, typename M, int VE, int NV>
+inline void* coop_fn() {
+  return reinterpret_cast<void*>(sgn_nhwc_coop<T, M, VE, NV>);
+}
+
+template <typename T, typename M>
+inline void* pick_coop(int ve, int nv) {
+  constexpr int V16 = static_cast<int>(16 / sizeof(T));
+  if (ve == 1) {
+    switch (nv) {
+      case 1: return coop_fn<T, M, 1, 1>();
+      case 2: return coop_fn<T, M, 1, 2>();
+      case 4: return coop_fn<T, M, 1, 4>();
+      case 8: return coop_fn<T, M, 1, 8>();
+    }
+    return nullptr;
+  }
+  switch (nv) {
+    case 1: return coop_fn<T, M, V16, 1>();
+    case 2: return coop_fn<T, M, V16, 2>();
+    case 4: return coop_fn<T, M, V16, 4>();
+    case 8: return coop_fn<T, M, V16, 8>();
+  }
+  return nullptr;
+}
+
+template <typename T, typename M>
+inline void* pick_resident(int ve) {
+  constexpr int V16 = static_cast<int>(16 / sizeof(T));
+  return ve == 1 ? reinterpret_cast<void*>(sgn_nchw_smem<T, M, 1>)
+                 : reinterpret_cast<void*>(sgn_nchw_smem<T, M, V16>);
+}
+
+template <typename T, typename M>
+inline cudaError_t launch_group_typed(const SkipGroupCall& c, const GroupPlan& p,
+                                      cudaStream_t stream) {
+  SgnArgs<T, M> a;
+  a.x = static_cast<const T*>(c.x);
+  a.skip = static_cast<const T*>(c.skip);
+  a.bias = static_cast<const T*>(c.bias);
+  a.gamma = static_cast<const M*>(c.gamma);
+  a.beta = static_cast<const M*>(c.beta);
+  a.y = static_cast<T*>(c.y);
+  a.s = static_cast<T*>(c.s);
+  a.N = c.N;
+  a.C = static_cast<int>(c.C);
+  a.HW = static_cast<int>(c.H * c.W);
+  a.cpg = static_cast<int>(c.C / c.groups);
+  a.groups = c.groups;
+  a.bcast = c.bcast ? 1 : 0;
+  a.act = c.activation;
+  a.eps = c.eps;
+  a.ctl = static_cast<Control*>(c.workspace);
+  a.part = reinterpret_cast<float4*>(static_cast<char*>(c.workspace) + kControlBytes);
+  a.limit_ns = kWaitLimitNs;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+  cfg.blockDim = dim3(p.block);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+
+  if (p.route == 1) {
+    void* fn = pick_resident<T, M>(p.ve);
+    if (!fn) return cudaErrorInvalidConfiguration;
+    unsigned nattr = 0;
+    if (p.csize > 1) {
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = p.csize;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      nattr = 1;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = add_pdl_attr(attr, nattr);
+    int span = p.nv;
+    FastDiv vpc = make_fastdiv(static_cast<unsigned>(a.HW / p.ve));
+    void* args[] = {&a, &span, &vpc};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+  }
+  if (p.route == 2) {
+    // A cooperative launch keeps plain stream order (no early scheduling).
+    void* fn = pick_coop<T, M>(p.ve, p.nv);
+    if (!fn) return cudaErrorInvalidConfiguration;
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int B = p.ctas_per_item, ppc = p.pix_per_cta;
+    const int PL = p.block / static_cast<int>(c.C / p.ve);
+    int koff = static_cast<int>(coop_k_offset(PL, static_cast<int>(c.C), B, c.groups));
+    void* args[] = {&a, &B, &ppc, &koff};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+  }
+  // route 3
+  int chunks = p.chunks;
+  cfg.attrs = attr;
+  cfg.numAttrs = add_pdl_attr(attr, 0);
+  void* args[] = {&a, &chunks};
+  void* first = c.channels_last ? reinterpret_cast<void*>(sgn_partials<T, M, true>)
+                                : reinterpret_cast<void*>(sgn_partials<T, M, false>);
+  void* second = c.channels_last ? reinterpret_cast<void*>(sgn_normalize<T, M, true>)
+                                 : reinterpret_cast<void*>(sgn_normalize<T, M, false>);
+  cudaError_t e = cudaLaunchKernelExC(&cfg, first, args);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelExC(&cfg, second, args);
+}
+
+// Kernel pointers and typed launches per element type T of X (group_f32.cu,
+// group_f16.cu, group_bf16.cu).  Pointers are null for (M, ve, nv) without
+// an instantiation.
+void* group_coop_kernel_f32(DType m, int ve, int nv);
+void* group_coop_kernel_f16(DType m, int ve, int nv);
+void* group_coop_kernel_bf16(DType m, int ve, int nv);
+void* group_resident_kernel_f32(DType m, int ve);
+void* group_resident_kernel_f16(DType m, int ve);
+void* group_resident_kernel_bf16(DType m, int ve);
+cudaError_t launch_group_f32(const SkipGroupCall& c, const GroupPlan& p, cudaStream_t stream);
+cudaError_t launch_group_f16(const SkipGroupCall& c, const GroupPlan& p, cudaStream_t stream);
+cudaError_t launch_group_bf16(const SkipGroupCall& c, const GroupPlan& p, cudaStream_t stream);
+
+}  // namespace b200norm

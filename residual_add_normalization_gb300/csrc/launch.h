@@ -43,7 +43,7 @@ class PlanCache {
   int next_ = 0;
 };
 
-enum class DType { F32 = 0, F16 = 1 };
+enum class DType { F32 = 0, F16 = 1, BF16 = 2 };
 
 inline size_t dtype_size(DType t) { return t == DType::F32 ? 4 : 2; }
 

@@ -1,5 +1,5 @@
 // GatedRMSNorm row kernels (float32 and float16), the row planner, and the
-// SkipSimplifiedLayerNormalization type switch.
+// element-type switches of both row operators.
 #include "rows_ops.cuh"
 
 #ifndef B200NORM_SHORT_RPG
@@ -87,12 +87,23 @@ RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok) {
 }
 
 cudaError_t launch_skip_rms(const SkipRmsCall& c, const RowPlan& p, cudaStream_t st) {
-  return c.t == DType::F32 ? skip_rms_f32(c, p, st) : skip_rms_f16(c, p, st);
+  switch (c.t) {
+    case DType::F32: return skip_rms_f32(c, p, st);
+    case DType::F16: return skip_rms_f16(c, p, st);
+    case DType::BF16: return skip_rms_bf16(c, p, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gated(const GatedCall& c, const RowPlan& p, cudaStream_t st) {
-  if (c.t == DType::F32) return p.ve == 4 ? gated_go<float, 4>(c, p, st) : gated_go<float, 1>(c, p, st);
-  return p.ve == 8 ? gated_go<__half, 8>(c, p, st) : gated_go<__half, 1>(c, p, st);
+  switch (c.t) {
+    case DType::F32:
+      return p.ve == 4 ? gated_go<float, 4>(c, p, st) : gated_go<float, 1>(c, p, st);
+    case DType::F16:
+      return p.ve == 8 ? gated_go<__half, 8>(c, p, st) : gated_go<__half, 1>(c, p, st);
+    case DType::BF16: return gated_bf16(c, p, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace b200norm

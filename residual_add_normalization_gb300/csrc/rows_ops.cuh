@@ -64,5 +64,7 @@ cudaError_t gated_go(const GatedCall& c, const RowPlan& plan, cudaStream_t st) {
 
 cudaError_t skip_rms_f32(const SkipRmsCall& c, const RowPlan& p, cudaStream_t st);
 cudaError_t skip_rms_f16(const SkipRmsCall& c, const RowPlan& p, cudaStream_t st);
+cudaError_t skip_rms_bf16(const SkipRmsCall& c, const RowPlan& p, cudaStream_t st);
+cudaError_t gated_bf16(const GatedCall& c, const RowPlan& p, cudaStream_t st);
 
 }  // namespace b200norm

@@ -30,6 +30,10 @@ deviation ``s``.
                        4096), distributions as ssln_fp16_8x2048x4096; seeds 5, 6.
   gated_fp16_decode_64x8192_c8192  decode-shaped GatedRMSNorm fp16, X/gate
                        (64, 8192) N(0,1), C = 8192; seed 7.
+  ssln_bf16_8x2048x4096, gated_bf16_4x4096x8192_c128,
+  sgn_nhwc_bf16_2x64x64x320, sgn_nchw_bf16_16x1280x16x16  bfloat16 variants
+                       of the large workloads (the NCHW one with bfloat16
+                       gamma/beta); seeds 8-11.
 
 bfloat16 host arrays are uint16 bit patterns whose dtype is ``BFLOAT16`` (a
 uint16 dtype carrying the metadata {"bfloat16": True}); values are drawn in
@@ -88,6 +92,21 @@ WORKLOADS = {
     "gated_fp16_decode_64x8192_c8192": dict(
         op="gated_rms", seed=7, dtype=np.float16, shape=(64, 8192), C=8192,
         epsilon=1e-5),
+    # bfloat16 variants of the large workloads (same shapes and distributions).
+    "ssln_bf16_8x2048x4096": dict(
+        op="skip_rms", seed=8, dtype=BFLOAT16, shape=(8, 2048, 4096), bias=True,
+        gamma=("normal", 1.0, 0.1), epsilon=SSLN_EPS, want_sum=True),
+    "gated_bf16_4x4096x8192_c128": dict(
+        op="gated_rms", seed=9, dtype=BFLOAT16, shape=(4, 4096, 8192), C=128,
+        epsilon=1e-5),
+    "sgn_nhwc_bf16_2x64x64x320": dict(
+        op="skip_group", seed=10, dtype=BFLOAT16, mdtype=np.float32,
+        shape=(2, 64, 64, 320), channels_last=1, skip="nc", bias=True, x_std=1.0,
+        groups=32, epsilon=1e-5, activation=1, want_sum=True),
+    "sgn_nchw_bf16_16x1280x16x16": dict(
+        op="skip_group", seed=11, dtype=BFLOAT16, mdtype=BFLOAT16,
+        shape=(16, 1280, 16, 16), channels_last=0, skip="full", bias=False, x_std=2.0,
+        groups=32, epsilon=1e-5, activation=0, want_sum=False),
 }
 
 # Order the workloads are listed in (small SSLN first, decode shapes last).

@@ -76,7 +76,7 @@ def ssln(lib, **kw):
 
 
 def test_skip_rms_validation(lib):
-    assert ssln(lib, T=2) == UNSUPPORTED                    # bfloat16 is not implemented
+    assert ssln(lib, T=3) == UNSUPPORTED                    # no such element type
     assert ssln(lib, rows=-1) == INVALID
     assert ssln(lib, hidden=0) == INVALID
     assert ssln(lib, eps=-1.0) == INVALID                   # epsilon is non-negative
@@ -125,7 +125,10 @@ def test_skip_group_validation(lib):
     assert sgn(lib, act=2) == INVALID               # activation is 0 or 1
     assert sgn(lib, act=-1) == INVALID
     assert sgn(lib, eps=-1.0) == INVALID
-    assert sgn(lib, M=2) == UNSUPPORTED
+    assert sgn(lib, M=2) == UNSUPPORTED             # bfloat16 gamma under float16 X
+    assert sgn(lib, T=2, M=1) == UNSUPPORTED        # float16 gamma under bfloat16 X
+    assert sgn(lib, T=0, M=2) == UNSUPPORTED
+    assert sgn(lib, T=3, M=0) == UNSUPPORTED
     assert sgn(lib, rank=2, dims=(2, 4, 0, 0)) == INVALID          # skip (N, C') wrong
     assert sgn(lib, rank=3, dims=(2, 1, 8, 0)) == INVALID
     assert sgn(lib, rank=4, dims=(2, 3, 2, 4)) == INVALID          # not X's shape

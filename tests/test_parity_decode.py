@@ -40,7 +40,7 @@ def _force(csize, nv):
     assert b2.library().b200norm_testing_force_split(csize, nv) == 0
 
 
-@pytest.mark.parametrize("dtype", [np.float16, np.float32])
+@pytest.mark.parametrize("dtype", [np.float16, np.float32, synthetic.BFLOAT16])
 @pytest.mark.parametrize("rows,hidden", [(1, 4096), (3, 8192), (16, 4096), (2, 5000)])
 @pytest.mark.parametrize("split", SPLITS)
 def test_decode_skip_rms_forced_splits(dtype, rows, hidden, split):
@@ -59,7 +59,7 @@ def test_decode_skip_rms_forced_splits(dtype, rows, hidden, split):
     assert_y_close(to_host(y), ry)
 
 
-@pytest.mark.parametrize("dtype", [np.float16, np.float32])
+@pytest.mark.parametrize("dtype", [np.float16, np.float32, synthetic.BFLOAT16])
 @pytest.mark.parametrize("rows,C", [(1, 8192), (4, 4096), (2, 2056)])
 @pytest.mark.parametrize("split", SPLITS)
 def test_decode_gated_forced_splits(dtype, rows, C, split):

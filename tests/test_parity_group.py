@@ -74,8 +74,12 @@ NCHW_CASES = [
 ]
 
 
-@pytest.mark.parametrize("dtype,mdtype", [(np.float32, np.float16), (np.float16, np.float32),
-                                          (np.float16, np.float16), (np.float32, np.float32)])
+BF16 = synthetic.BFLOAT16
+TYPE_PAIRS = [(np.float32, np.float16), (np.float16, np.float32), (np.float16, np.float16),
+              (np.float32, np.float32), (BF16, np.float32), (BF16, BF16)]
+
+
+@pytest.mark.parametrize("dtype,mdtype", TYPE_PAIRS)
 @pytest.mark.parametrize("case", NCHW_CASES)
 def test_nchw_matches_oracle(dtype, mdtype, case):
     N, C, H, W, G = case
@@ -100,8 +104,7 @@ NHWC_CASES = [
 ]
 
 
-@pytest.mark.parametrize("dtype,mdtype", [(np.float16, np.float32), (np.float32, np.float16),
-                                          (np.float16, np.float16), (np.float32, np.float32)])
+@pytest.mark.parametrize("dtype,mdtype", TYPE_PAIRS)
 @pytest.mark.parametrize("case", NHWC_CASES)
 def test_nhwc_matches_oracle(dtype, mdtype, case):
     N, H, W, C, G = case
@@ -113,7 +116,7 @@ def test_nhwc_matches_oracle(dtype, mdtype, case):
 
 
 @pytest.mark.parametrize("cl", [0, 1])
-@pytest.mark.parametrize("dtype", [np.float32, np.float16])
+@pytest.mark.parametrize("dtype", [np.float32, np.float16, BF16])
 def test_forced_two_phase(cl, dtype):
     assert b2.library().b200norm_testing_force(0, 3) == 0
     shape = (2, 16, 16, 64) if cl else (2, 64, 16, 16)

@@ -15,9 +15,12 @@ import torch
 import oracle
 import residual_add_normalization_gb300 as b2
 from residual_add_normalization_gb300 import synthetic
+import helpers
 from helpers import assert_bitexact, assert_y_close, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
+
+DTYPES = [np.float32, np.float16, synthetic.BFLOAT16]
 
 
 def _plan(n, T, rows=4):
@@ -39,7 +42,7 @@ def _dev(a, shift):
         return None
     if not shift:
         return to_dev(a)
-    t = torch.from_numpy(np.ascontiguousarray(a))
+    t = to_dev(a, "cpu")
     flat = torch.empty(a.size + shift, dtype=t.dtype, device="cuda")
     v = flat[shift:].view(a.shape)
     v.copy_(t)
@@ -66,7 +69,7 @@ SSLN_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("dtype", [np.float32, np.float16])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("shape", SSLN_SHAPES)
 @pytest.mark.parametrize("bias,want_sum", [(True, True), (False, False), (True, False)])
 def test_skip_rms_matches_oracle(dtype, shape, bias, want_sum):
@@ -82,7 +85,7 @@ def test_skip_rms_matches_oracle(dtype, shape, bias, want_sum):
     assert_y_close(y, ry)
 
 
-@pytest.mark.parametrize("dtype", [np.float32, np.float16])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("shape", [(4, 4096), (6, 200), (3, 7)])
 def test_skip_rms_unaligned_scalar_path(dtype, shape):
     d = synthetic.skip_rms_inputs(shape, dtype, seed=3, bias=True)
@@ -92,7 +95,7 @@ def test_skip_rms_unaligned_scalar_path(dtype, shape):
     assert_y_close(y, ry)
 
 
-@pytest.mark.parametrize("dtype", [np.float32, np.float16])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("shape", [(5, 4096), (7, 24), (2, 33000)])
 def test_skip_rms_forced_walk(dtype, shape):
     assert b2.library().b200norm_testing_force(2, 0) == 0
@@ -103,7 +106,7 @@ def test_skip_rms_forced_walk(dtype, shape):
     assert_y_close(y, ry)
 
 
-@pytest.mark.parametrize("dtype", [np.float32, np.float16])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("shape", [(6, 40), (3, 4096), (2, 70000)])
 def test_skip_rms_stats_outputs(dtype, shape):
     d = synthetic.skip_rms_inputs(shape, dtype, seed=8, bias=True)
@@ -132,6 +135,27 @@ def test_skip_rms_edge_values():
         assert_bitexact(s, rs)
         assert_y_close(y, ry)
         assert np.isnan(y[0]).all()
+
+
+def test_skip_rms_edge_values_bf16():
+    """bfloat16: zero rows with eps = 0 give NaN on both sides, -0 survives an
+    absent bias, and values up to 1e18 (squares far beyond float16's range,
+    row sums of squares still finite in float32) give matching S and Y."""
+    x = np.zeros((4, 64), np.float32)
+    x[1] = -0.0
+    x[2] = 1e18
+    x[2, 1::2] = -3e17
+    x[3, ::2] = -3.5
+    sk = x.copy()
+    sk[2] = 0.5
+    x, sk = synthetic.to_bfloat16(x), synthetic.to_bfloat16(sk)
+    g = synthetic.to_bfloat16(np.ones(64, np.float32))
+    for bias in (None, synthetic.to_bfloat16(np.zeros(64, np.float32))):
+        y, s = run_ssln(dict(input=x, skip=sk, gamma=g, bias=bias), 0.0)
+        ry, rs = oracle.skip_rms(x, sk, g, bias, epsilon=0.0)
+        assert_bitexact(s, rs)
+        assert_y_close(y, ry)
+        assert np.isnan(helpers.values(y[0])).all()
 
 
 def test_skip_rms_empty_rows():
@@ -173,7 +197,7 @@ GATED_CASES = [
 ]
 
 
-@pytest.mark.parametrize("dtype", [np.float32, np.float16])
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("shape,C", GATED_CASES)
 def test_gated_matches_oracle(dtype, shape, C):
     d = synthetic.gated_rms_inputs(shape, C, dtype, seed=C % 97)
@@ -190,7 +214,7 @@ def test_gated_scale_spellings(spelling):
     assert_y_close(y, ry)
 
 
-@pytest.mark.parametrize("dtype", [np.float32, np.float16])
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_gated_forced_walk(dtype):
     assert b2.library().b200norm_testing_force(2, 0) == 0
     d = synthetic.gated_rms_inputs((4, 1024), 128, dtype, seed=6)
