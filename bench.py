@@ -169,7 +169,8 @@ def make_calls(torch, b2, dev, names=None, rotate=True):
                 shape = spec["shape"]
                 N, C, H, W = ((shape[0], shape[3], shape[1], shape[2]) if spec["channels_last"]
                               else shape)
-                ws = torch.zeros(b2.workspace_size(N, C, H, W, spec["groups"]),
+                ws = torch.zeros(b2.workspace_size(N, C, H, W, spec["groups"], t["x"].dtype,
+                                                   spec["channels_last"]),
                                  dtype=torch.uint8, device=dev)
                 def fn(t=t, y=y, s=s, spec=spec, ws=ws):
                     b2.skip_group(t["x"], t["skip"], t["gamma"], t["beta"], t["bias"],

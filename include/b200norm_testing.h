@@ -24,8 +24,12 @@ B200NORM_API b200norm_status b200norm_testing_barrier_timeout(void* workspace,
 
 /* Force a schedule on the calling thread (0 = automatic choice):
  *   row_mode:    2 = walk each row twice (any row length)
- *   group_route: 3 = two-phase partials -> normalize (any shape)
- * Other values are rejected with B200NORM_ERR_INVALID_ARGUMENT. */
+ *   group_route: 2 = NHWC cooperative grid with one bounded grid barrier
+ *                3 = two-phase partials -> normalize (any shape)
+ *                4 = NHWC through L2 (statistics kernel, then apply kernel)
+ * Other values are rejected with B200NORM_ERR_INVALID_ARGUMENT.  A later
+ * SkipGroupNorm call that the forced route cannot take returns
+ * B200NORM_ERR_UNSUPPORTED. */
 B200NORM_API b200norm_status b200norm_testing_force(int row_mode, int group_route);
 
 /* Force the row schedule of SkipSimplifiedLayerNormalization and

@@ -272,8 +272,9 @@ b200norm_status b200norm_gated_rms(const void* x, const void* gate, const void* 
 }
 
 size_t b200norm_skip_group_workspace_size(int64_t N, int64_t C, int64_t H, int64_t W, int groups,
-                                          b200norm_dtype /*T*/, int /*channels_last*/) {
-  return group_workspace_bytes(N, C, H, W, groups);
+                                          b200norm_dtype T, int /*channels_last*/) {
+  if (!dtype_ok(T)) return kControlBytes;
+  return group_workspace_bytes(N, C, H, W, groups, to_dtype(T));
 }
 
 b200norm_status b200norm_skip_group(const void* x, const void* skip, int skip_rank,
@@ -304,7 +305,7 @@ b200norm_status b200norm_skip_group(const void* x, const void* skip, int skip_ra
     return fail(B200NORM_ERR_UNSUPPORTED, "C, H*W or N exceeds 2^31-1");
   if (!x || !skip || !gamma || !beta || !y)
     return fail(B200NORM_ERR_INVALID_ARGUMENT, "x, skip, gamma, beta and y are required");
-  const size_t need = group_workspace_bytes(N, C, H, W, groups);
+  const size_t need = group_workspace_bytes(N, C, H, W, groups, to_dtype(T));
   if (!workspace || workspace_bytes < need)
     return fail(B200NORM_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu at %p)", need,
                 workspace_bytes, workspace);
@@ -331,9 +332,11 @@ b200norm_status b200norm_skip_group(const void* x, const void* skip, int skip_ra
   for (const void* p : tptrs)
     if (p && !aligned(p, 16)) vec = false;
   GroupPlan plan;
-  cudaError_t e = plan_group(c, vec, &plan);
+  cudaError_t e = plan_group(c, vec, g_force_group_route, &plan);
+  if (e == cudaErrorNotSupported && g_force_group_route)
+    return fail(B200NORM_ERR_UNSUPPORTED, "forced route %d cannot take this call",
+                g_force_group_route);
   if (e != cudaSuccess) return cuda_fail(e, "skip_group planning");
-  if (g_force_group_route == 3) plan = two_phase_plan(c);
   if (plan.grid > kMaxGrid) return fail(B200NORM_ERR_UNSUPPORTED, "problem too large for one launch");
   e = launch_group(c, plan, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
@@ -383,8 +386,9 @@ b200norm_status b200norm_testing_barrier_timeout(void* workspace, size_t workspa
 }
 
 b200norm_status b200norm_testing_force(int row_mode, int group_route) {
-  if ((row_mode != 0 && row_mode != 2) || (group_route != 0 && group_route != 3))
-    return fail(B200NORM_ERR_INVALID_ARGUMENT, "row_mode in {0, 2}, group_route in {0, 3}");
+  if ((row_mode != 0 && row_mode != 2) ||
+      (group_route != 0 && group_route != 2 && group_route != 3 && group_route != 4))
+    return fail(B200NORM_ERR_INVALID_ARGUMENT, "row_mode in {0, 2}, group_route in {0, 2, 3, 4}");
   g_force_row_mode = row_mode;
   g_force_group_route = group_route;
   return ok();
@@ -435,7 +439,7 @@ b200norm_status b200norm_testing_plan_group(int64_t N, int64_t C, int64_t H, int
   c.m = to_dtype(M);
   c.channels_last = channels_last != 0;
   GroupPlan p;
-  cudaError_t e = plan_group(c, aligned16 != 0, &p);
+  cudaError_t e = plan_group(c, aligned16 != 0, 0, &p);
   if (e != cudaSuccess) return cuda_fail(e, "plan_group");
   const int64_t v[8] = {p.route, p.ve, p.nv, p.block, p.csize, p.grid, p.ctas_per_item,
                         p.pix_per_cta};

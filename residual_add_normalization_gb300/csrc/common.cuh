@@ -302,12 +302,17 @@ __device__ __forceinline__ void pdl_trigger() {
 
 // ---------------------------------------------------------------------------
 // Control block at the start of a SkipGroupNorm workspace.
+// Every counter is zero between calls (each call that uses one returns it to
+// zero), so one workspace serves calls of any shape in turn.
+constexpr int kL2MaxItems = 56;  // batch items of the NHWC L2 route
 struct Control {
   unsigned int bar_count;  // CTAs arrived at the current barrier (0 between barriers)
   unsigned int bar_gen;    // barrier generation
   unsigned int error;      // 0, or a b200norm_status recorded by a kernel
   unsigned int error_site; // which wait gave up
+  unsigned int item_done[kL2MaxItems];  // NHWC L2 route: CTAs of item n done
 };
+static_assert(sizeof(Control) <= 256, "the control block is 256 bytes");
 
 constexpr unsigned kStatusDeviceTimeout = 5;  // B200NORM_ERR_DEVICE_TIMEOUT
 

@@ -69,6 +69,35 @@ __device__ __forceinline__ T sgn_sum(float x, float sk, const T* __restrict__ bi
   return from_f32<T>(t);
 }
 
+// The same with the bias value already loaded (ignored when has_bias is
+// false: then there is no add at all).
+template <typename T>
+__device__ __forceinline__ T sgn_sum_b(float x, float sk, float b, bool has_bias) {
+  float t = __fadd_rn(x, sk);
+  if (has_bias) t = __fadd_rn(t, b);
+  return from_f32<T>(t);
+}
+
+// VE consecutive floats of shared memory at a 16-byte aligned address, read
+// as 16-byte vectors where VE allows: threads that read VE floats apart meet
+// far fewer bank conflicts than with VE scalar reads.
+template <int VE>
+__device__ __forceinline__ void lds_vec(const float* p, float (&out)[VE]) {
+  if constexpr (VE % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < VE / 4; ++i) {
+      const float4 v = reinterpret_cast<const float4*>(p)[i];
+      out[4 * i] = v.x;
+      out[4 * i + 1] = v.y;
+      out[4 * i + 2] = v.z;
+      out[4 * i + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < VE; ++e) out[e] = p[e];
+  }
+}
+
 // ((S - K) - d) * rstd * gamma + beta, then SiLU when requested.
 __device__ __forceinline__ float sgn_out(float s, float K, float d, float rstd, float ga,
                                          float be, int act) {
@@ -246,10 +275,11 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
       if (!a.bcast) kv[k] = ld_stream<T, VE>(a.skip + off);
     }
   }
-  Pack<T, VE> skb;
+  Pack<T, VE> skb, bv;
   if (a.bcast) skb = ld_reuse<T, VE>(a.skip + static_cast<int64_t>(n) * C + c0);
+  if (a.bias) bv = ld_reuse<T, VE>(a.bias + c0);
   // the affine weights are needed only at the end: stage them now
-  float* s_ga = s_K + a.groups;
+  float* s_ga = s_K + ((a.groups + 3) & ~3);  // 16-byte aligned
   float* s_be = s_ga + C;
   for (int c = threadIdx.x; c < C; c += blockDim.x) {
     s_ga[c] = to_f32(__ldg(a.gamma + c));
@@ -270,7 +300,7 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
 #pragma unroll
       for (int e = 0; e < VE; ++e) {
         const float sk = a.bcast ? to_f32(skb.v[e]) : to_f32(kv[k].v[e]);
-        sv[k].v[e] = sgn_sum<T>(to_f32(xv[k].v[e]), sk, a.bias, c0 + e);
+        sv[k].v[e] = sgn_sum_b<T>(to_f32(xv[k].v[e]), sk, to_f32(bv.v[e]), a.bias != nullptr);
         lsum[e] += to_f32(sv[k].v[e]) - Kl[e];
       }
     }
@@ -378,11 +408,266 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
     if (p < p1) {
       const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
       if (a.s) st_stream<T, VE>(a.s + off, sv[k]);
+      float ga[VE], be[VE];
+      lds_vec<VE>(s_ga + c0, ga);
+      lds_vec<VE>(s_be + c0, be);
       Pack<T, VE> out;
 #pragma unroll
       for (int e = 0; e < VE; ++e)
-        out.v[e] = from_f32<T>(sgn_out(to_f32(sv[k].v[e]), Kl[e], mu[e], rs[e],
-                                       s_ga[c0 + e], s_be[c0 + e], a.act));
+        out.v[e] = from_f32<T>(sgn_out(to_f32(sv[k].v[e]), Kl[e], mu[e], rs[e], ga[e], be[e],
+                                       a.act));
+      st_stream<T, VE>(a.y + off, out);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Route 4: NHWC through L2, two kernels
+// ---------------------------------------------------------------------------
+// For NHWC tensors small enough to stay in L2 between two kernels.  Both
+// kernels map blockDim.x = CV * PL threads like route 2 (thread t covers the
+// VE channels (t % CV) * VE .. +VE of pixel lane t / CV) and give CTA b of
+// batch item n = b / B the pixels [(b % B) * kL2Passes * PL, +kL2Passes * PL).
+//
+// sgn_nhwc_stats forms S (not stored) and accumulates, per group, the sums of
+// S - K[g] and (S - K[g])^2 over its pixels (K[g] the group's first residual
+// sum, the same for every CTA), and writes them to the workspace.  The last
+// CTA of a batch item to finish (counted with an atomic) adds the item's B
+// partials in a fixed order and writes each group's (K, d, rstd):
+// mean = K + d, var = sum((S-K)^2)/n - d^2.  X and skip are read with the
+// default cache policy so that the second kernel finds them in L2.
+//
+// sgn_nhwc_apply loads its inputs before waiting for the first kernel (it
+// writes none of them), then reads the group statistics, re-forms S, and
+// stores S and Y.
+//
+// Workspace: float4 slots after the control block hold the partials
+// [N * B * groups] and the statistics [N * groups]; the control block holds
+// one counter per batch item (N <= kL2MaxItems), zero between calls.
+constexpr int kL2Passes = 4;       // pixels per thread, statistics kernel
+constexpr int kL2ApplyPasses = 4;  // pixels per thread, apply kernel
+constexpr int kL2MaxThreads = 512;
+constexpr int64_t kL2RouteMaxBytes = 48ll << 20;  // re-read through the 129 MB L2
+constexpr int64_t kL2MaxPartials = 1ll << 20;     // workspace partial slots
+
+template <typename T, typename M, int VE, bool BC>
+__global__ void __launch_bounds__(kL2MaxThreads, 2)
+sgn_nhwc_stats(const SgnArgs<T, M> a, int B) {
+  pdl_wait();
+  pdl_trigger();
+  // s_red: per-thread sums [2][VE][PL][CV], later the merge slices [3][S][groups]
+  constexpr int kRed = 2 * kL2MaxThreads * VE > 3 * 1024 ? 2 * kL2MaxThreads * VE : 3 * 1024;
+  __shared__ float s_red[kRed];
+  __shared__ float s_col[2 * 1024];  // [2][C], C <= 1024
+  __shared__ unsigned s_last;
+  extern __shared__ float s_K[];  // [groups]
+  const int C = a.C;
+  const int CV = C / VE;
+  const int PL = blockDim.x / CV;
+  const int tc = threadIdx.x % CV;
+  const int tp = threadIdx.x / CV;
+  const int n = blockIdx.x / B;
+  const int b = blockIdx.x % B;
+  const int p0 = b * kL2Passes * PL;
+  const int p1 = min(p0 + kL2Passes * PL, a.HW);
+  const int64_t nbase = static_cast<int64_t>(n) * a.HW * C;
+  const int c0 = tc * VE;
+  const bool active = tp < PL;
+
+  Pack<T, VE> xv[kL2Passes], kv[BC ? 1 : kL2Passes], skb, bv;
+  if (active) {
+#pragma unroll
+    for (int k = 0; k < kL2Passes; ++k) {
+      const int p = p0 + tp + k * PL;
+      if (p < p1) {
+        const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+        xv[k] = ld_reuse<T, VE>(a.x + off);
+        if constexpr (!BC) kv[k] = ld_reuse<T, VE>(a.skip + off);
+      }
+    }
+    if constexpr (BC) skb = ld_reuse<T, VE>(a.skip + static_cast<int64_t>(n) * C + c0);
+    if (a.bias) bv = ld_reuse<T, VE>(a.bias + c0);
+  }
+  for (int g = threadIdx.x; g < a.groups; g += blockDim.x) s_K[g] = sgn_shift(a, n, g, true);
+  __syncthreads();
+  float s1[VE], s2[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) s1[e] = s2[e] = 0.0f;
+  if (active) {
+    float Kl[VE];
+#pragma unroll
+    for (int e = 0; e < VE; ++e) Kl[e] = s_K[(c0 + e) / a.cpg];
+#pragma unroll
+    for (int k = 0; k < kL2Passes; ++k) {
+      const int p = p0 + tp + k * PL;
+      if (p < p1) {
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          const float sk = BC ? to_f32(skb.v[e]) : to_f32(kv[BC ? 0 : k].v[e]);
+          const float d =
+              to_f32(sgn_sum_b<T>(to_f32(xv[k].v[e]), sk, to_f32(bv.v[e]), a.bias != nullptr)) -
+              Kl[e];
+          s1[e] += d;
+          s2[e] = fmaf(d, d, s2[e]);
+        }
+      }
+    }
+  }
+  // per channel (over the pixel lanes), then per group
+  const int nthr = PL * CV;
+  if (active) {
+#pragma unroll
+    for (int e = 0; e < VE; ++e) {
+      s_red[(e * PL + tp) * CV + tc] = s1[e];
+      s_red[nthr * VE + (e * PL + tp) * CV + tc] = s2[e];
+    }
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < C; j += blockDim.x) {
+    const int e = j / CV, q0 = j % CV;
+    float t1 = 0.0f, t2 = 0.0f;
+    for (int q = 0; q < PL; ++q) {
+      t1 += s_red[(e * PL + q) * CV + q0];
+      t2 += s_red[nthr * VE + (e * PL + q) * CV + q0];
+    }
+    s_col[q0 * VE + e] = t1;
+    s_col[C + q0 * VE + e] = t2;
+  }
+  __syncthreads();
+  const float cnt = static_cast<float>(p1 - p0) * static_cast<float>(a.cpg);
+  float4* part = a.part + static_cast<int64_t>(n) * B * a.groups;
+  for (int g = threadIdx.x; g < a.groups; g += blockDim.x) {
+    float t1 = 0.0f, t2 = 0.0f;
+    for (int cc = 0; cc < a.cpg; ++cc) {
+      t1 += s_col[g * a.cpg + cc];
+      t2 += s_col[C + g * a.cpg + cc];
+    }
+    part[static_cast<int64_t>(b) * a.groups + g] = make_float4(t1, t2, cnt, 0.0f);
+  }
+  // The last CTA of this batch item merges its partials.  The barrier orders
+  // every thread's partial stores before thread 0's fence, and the fence
+  // (cumulative) makes them visible GPU-wide before the count goes up; on
+  // the merging side the fence after the count orders the reads after it.
+  __syncthreads();
+  float4* stats = a.part + a.N * B * a.groups;
+  unsigned* counter = a.ctl->item_done + n;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(counter, 1u) == static_cast<unsigned>(B - 1);
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // Slice j of group g adds partials j, j + S, j + 2S, ... (S slices per
+  // group, the block's threads spread over groups x slices); the slices are
+  // then added in order, so the result does not depend on which CTA merges.
+  const int S = max(1, static_cast<int>(blockDim.x) / a.groups);
+  float* s_m = s_red;  // [3][S][groups]
+  for (int idx = threadIdx.x; idx < S * a.groups; idx += blockDim.x) {
+    const int g = idx % a.groups, j = idx / a.groups;
+    float t1 = 0.0f, t2 = 0.0f, c = 0.0f;
+    int q = j;
+    for (; q + 7 * S < B; q += 8 * S) {
+      float4 u[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) u[i] = __ldcg(part + static_cast<int64_t>(q + i * S) * a.groups + g);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        t1 += u[i].x;
+        t2 += u[i].y;
+        c += u[i].z;
+      }
+    }
+    for (; q < B; q += S) {
+      const float4 u = __ldcg(part + static_cast<int64_t>(q) * a.groups + g);
+      t1 += u.x;
+      t2 += u.y;
+      c += u.z;
+    }
+    s_m[(0 * S + j) * a.groups + g] = t1;
+    s_m[(1 * S + j) * a.groups + g] = t2;
+    s_m[(2 * S + j) * a.groups + g] = c;
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g < a.groups; g += blockDim.x) {
+    float t1 = 0.0f, t2 = 0.0f, c = 0.0f;
+    for (int j = 0; j < S; ++j) {
+      t1 += s_m[(0 * S + j) * a.groups + g];
+      t2 += s_m[(1 * S + j) * a.groups + g];
+      c += s_m[(2 * S + j) * a.groups + g];
+    }
+    const float d = t1 / c;
+    const float var = fmaxf(t2 / c - d * d, 0.0f);
+    stats[static_cast<int64_t>(n) * a.groups + g] =
+        make_float4(s_K[g], d, 1.0f / sqrtf(var + a.eps), 0.0f);
+  }
+  if (threadIdx.x == 0) *counter = 0u;  // ready for the next call
+}
+
+template <typename T, typename M, int VE, bool BC>
+__global__ void __launch_bounds__(kL2MaxThreads, 2)
+sgn_nhwc_apply(const SgnArgs<T, M> a, int B, int B2) {
+  extern __shared__ float4 s_st[];  // [groups] (K, d, rstd, -) | gamma[C] | beta[C]
+  float* s_ga = reinterpret_cast<float*>(s_st + a.groups);
+  float* s_be = s_ga + a.C;
+  const int C = a.C;
+  const int CV = C / VE;
+  const int PL = blockDim.x / CV;
+  const int tc = threadIdx.x % CV;
+  const int tp = threadIdx.x / CV;
+  const int n = blockIdx.x / B2;
+  const int b = blockIdx.x % B2;
+  const int p0 = b * kL2ApplyPasses * PL;
+  const int p1 = min(p0 + kL2ApplyPasses * PL, a.HW);
+  const int64_t nbase = static_cast<int64_t>(n) * a.HW * C;
+  const int c0 = tc * VE;
+  const bool active = tp < PL;
+  // Inputs first: the kernel before this one (the statistics kernel) writes
+  // none of them, and it waited for everything before it.
+  Pack<T, VE> xv[kL2ApplyPasses], kv[BC ? 1 : kL2ApplyPasses], skb, bv;
+  if (active) {
+#pragma unroll
+    for (int k = 0; k < kL2ApplyPasses; ++k) {
+      const int p = p0 + tp + k * PL;
+      if (p < p1) {
+        const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+        xv[k] = ld_stream<T, VE>(a.x + off);
+        if constexpr (!BC) kv[k] = ld_stream<T, VE>(a.skip + off);
+      }
+    }
+    if constexpr (BC) skb = ld_reuse<T, VE>(a.skip + static_cast<int64_t>(n) * C + c0);
+    if (a.bias) bv = ld_reuse<T, VE>(a.bias + c0);
+  }
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    s_ga[c] = to_f32(__ldg(a.gamma + c));
+    s_be[c] = to_f32(__ldg(a.beta + c));
+  }
+  pdl_wait();
+  pdl_trigger();
+  const float4* stats = a.part + a.N * B * a.groups + static_cast<int64_t>(n) * a.groups;
+  for (int g = threadIdx.x; g < a.groups; g += blockDim.x) s_st[g] = __ldcg(stats + g);
+  __syncthreads();
+  if (!active) return;
+  int gi[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) gi[e] = (c0 + e) / a.cpg;
+#pragma unroll
+  for (int k = 0; k < kL2ApplyPasses; ++k) {
+    const int p = p0 + tp + k * PL;
+    if (p < p1) {
+      const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+      Pack<T, VE> sv, out;
+      float ga[VE], be[VE];
+      lds_vec<VE>(s_ga + c0, ga);
+      lds_vec<VE>(s_be + c0, be);
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        const float sk = BC ? to_f32(skb.v[e]) : to_f32(kv[BC ? 0 : k].v[e]);
+        sv.v[e] = sgn_sum_b<T>(to_f32(xv[k].v[e]), sk, to_f32(bv.v[e]), a.bias != nullptr);
+        const float4 st = s_st[gi[e]];
+        out.v[e] = from_f32<T>(sgn_out(to_f32(sv.v[e]), st.x, st.y, st.z, ga[e], be[e], a.act));
+      }
+      if (a.s) st_stream<T, VE>(a.s + off, sv);
       st_stream<T, VE>(a.y + off, out);
     }
   }
@@ -535,7 +820,8 @@ inline size_t coop_k_offset(int PL, int C, int B, int groups) {
   const size_t passes = static_cast<size_t>(PL) * C + C + groups;
   const size_t nchunk = (static_cast<size_t>(B) + kCoopMergeChunk - 1) / kCoopMergeChunk;
   const size_t merge = nchunk * groups * 3 + 2ull * groups;
-  return passes > merge ? passes : merge;
+  const size_t off = passes > merge ? passes : merge;
+  return (off + 3) & ~static_cast<size_t>(3);  // 16-byte aligned tail
 }
 
 template <typename T, typename M, int VE, int NV>
@@ -569,6 +855,26 @@ inline void* pick_resident(int ve) {
   constexpr int V16 = static_cast<int>(16 / sizeof(T));
   return ve == 1 ? reinterpret_cast<void*>(sgn_nchw_smem<T, M, 1>)
                  : reinterpret_cast<void*>(sgn_nchw_smem<T, M, V16>);
+}
+
+// Route 4 kernels for vectors of `ve` elements and (N, C) or full skip:
+// {statistics, apply}.
+template <typename T, typename M, int VE>
+inline void pick_l2_ve(bool bcast, void** stats, void** apply) {
+  if (bcast) {
+    *stats = reinterpret_cast<void*>(sgn_nhwc_stats<T, M, VE, true>);
+    *apply = reinterpret_cast<void*>(sgn_nhwc_apply<T, M, VE, true>);
+  } else {
+    *stats = reinterpret_cast<void*>(sgn_nhwc_stats<T, M, VE, false>);
+    *apply = reinterpret_cast<void*>(sgn_nhwc_apply<T, M, VE, false>);
+  }
+}
+
+template <typename T, typename M>
+inline void pick_l2(int ve, bool bcast, void** stats, void** apply) {
+  constexpr int V16 = static_cast<int>(16 / sizeof(T));
+  if (ve == 1) pick_l2_ve<T, M, 1>(bcast, stats, apply);
+  else pick_l2_ve<T, M, V16>(bcast, stats, apply);
 }
 
 template <typename T, typename M>
@@ -632,6 +938,23 @@ inline cudaError_t launch_group_typed(const SkipGroupCall& c, const GroupPlan& p
     int koff = static_cast<int>(coop_k_offset(PL, static_cast<int>(c.C), B, c.groups));
     void* args[] = {&a, &B, &ppc, &koff};
     return cudaLaunchKernelExC(&cfg, fn, args);
+  }
+  if (p.route == 4) {
+    void *stats = nullptr, *apply = nullptr;
+    pick_l2<T, M>(p.ve, c.bcast, &stats, &apply);
+    int B = p.ctas_per_item;
+    const int PL = p.block / static_cast<int>(c.C / p.ve);
+    int B2 = static_cast<int>((c.H * c.W + kL2ApplyPasses * PL - 1) / (kL2ApplyPasses * PL));
+    void* args1[] = {&a, &B};
+    void* args2[] = {&a, &B, &B2};
+    cfg.attrs = attr;
+    cfg.numAttrs = add_pdl_attr(attr, 0);
+    cfg.dynamicSmemBytes = static_cast<size_t>(c.groups) * sizeof(float);
+    cudaError_t e = cudaLaunchKernelExC(&cfg, stats, args1);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(static_cast<unsigned>(c.N * B2));
+    cfg.dynamicSmemBytes = p.smem;
+    return cudaLaunchKernelExC(&cfg, apply, args2);
   }
   // route 3
   int chunks = p.chunks;

@@ -19,12 +19,39 @@ __global__ void barrier_timeout_probe(Control* ctl, unsigned long long limit_ns)
 // ---------------------------------------------------------------------------
 static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-size_t group_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int groups) {
+// Route 4 geometry for vectors of `ve` elements: false when the route does
+// not apply (channels per CTA row, shared-memory tables or partial count out
+// of range).  `in_bytes` is what the second kernel re-reads through L2.
+static bool l2_route_shape(int64_t N, int64_t C, int64_t HW, int groups, int ve,
+                           int64_t in_bytes, int* PL, int64_t* B) {
+  if (N > kL2MaxItems || C % ve != 0 || C > 1024 || in_bytes > kL2RouteMaxBytes) return false;
+  const int64_t CV = C / ve;
+  if (CV > kL2MaxThreads) return false;
+  *PL = static_cast<int>(kL2MaxThreads / CV);
+  *B = cdiv(HW, static_cast<int64_t>(kL2Passes) * *PL);
+  return N * *B * groups <= kL2MaxPartials;
+}
+
+// Workspace slots of route 4 (partials and statistics).
+static int64_t l2_route_slots(int64_t N, int64_t B, int groups) {
+  return N * B * groups + N * groups;
+}
+
+size_t group_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int groups, DType t) {
   if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || groups <= 0) return kControlBytes;
   const int64_t L = (C / groups) * H * W;
   const int64_t two_phase = N * groups * cdiv(L, kTwoPhaseChunk);
   const int64_t coop = static_cast<int64_t>(kMaxCoopCtas) * groups;
-  const int64_t slots = two_phase > coop ? two_phase : coop;
+  int64_t slots = two_phase > coop ? two_phase : coop;
+  const int64_t es = static_cast<int64_t>(dtype_size(t));
+  for (int ve : {1, static_cast<int>(16 / es)}) {
+    int PL = 0;
+    int64_t B = 0;
+    if (l2_route_shape(N, C, H * W, groups, ve, N * H * W * C * es, &PL, &B)) {
+      const int64_t r4 = l2_route_slots(N, B, groups);
+      if (r4 > slots) slots = r4;
+    }
+  }
   return kControlBytes + static_cast<size_t>(slots) * sizeof(float4);
 }
 
@@ -95,7 +122,7 @@ static bool allow_smem(void* fn, size_t smem, int dev) {
 
 // Offset (in floats) of the K[groups] tail of route 2's shared memory.
 static size_t coop_smem_bytes(int PL, int C, int B, int groups) {
-  return (coop_k_offset(PL, C, B, groups) + groups + 2ull * C) * sizeof(float);
+  return (coop_k_offset(PL, C, B, groups) + ((groups + 3) & ~3) + 2ull * C) * sizeof(float);
 }
 
 GroupPlan two_phase_plan(const SkipGroupCall& c) {
@@ -112,17 +139,47 @@ GroupPlan two_phase_plan(const SkipGroupCall& c) {
   return p;
 }
 
-static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, GroupPlan* p);
+// Route 4 for an NHWC call, if it applies (the tensors it re-reads stay in
+// L2 between its two kernels).
+static bool plan_l2_route(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) {
+  if (!c.channels_last) return false;
+  const int64_t es = static_cast<int64_t>(dtype_size(c.t));
+  const int vec = static_cast<int>(16 / es);
+  const int ve = (vector_ok && c.C % vec == 0) ? vec : 1;
+  const int64_t numel = c.N * c.H * c.W * c.C;
+  int PL = 0;
+  int64_t B = 0;
+  if (!l2_route_shape(c.N, c.C, c.H * c.W, c.groups, ve, numel * es * (c.bcast ? 1 : 2), &PL,
+                      &B))
+    return false;
+  *p = GroupPlan{};
+  p->route = 4;
+  p->ve = ve;
+  p->nv = kL2Passes;
+  p->block = static_cast<int>(PL * (c.C / ve));
+  p->csize = 1;
+  p->grid = c.N * B;
+  p->ctas_per_item = static_cast<int>(B);
+  p->pix_per_cta = kL2Passes * PL;
+  p->smem = static_cast<size_t>(c.groups) * sizeof(float4) + 2 * c.C * sizeof(float);
+  return true;
+}
 
-// Plans depend on the device, the shape, the types and the alignment only;
-// the occupancy queries behind them are costly, so they are cached.
+static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, int force,
+                                       GroupPlan* p);
+
+constexpr int64_t kCoopMergeMax = 3000;
+
+// Plans depend on the device, the shape, the types, the alignment and a
+// forced route only; the occupancy queries behind them are costly, so they
+// are cached.
 struct GroupPlanKey {
   int dev;
   int64_t N, C, H, W;
-  int groups, t, m, cl, vec;
+  int groups, t, m, cl, vec, bcast, force;
 };
 
-cudaError_t plan_group(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) {
+cudaError_t plan_group(const SkipGroupCall& c, bool vector_ok, int force_route, GroupPlan* p) {
   static PlanCache<GroupPlanKey, GroupPlan> cache;
   GroupPlanKey k;
   memset(&k, 0, sizeof(k));
@@ -137,14 +194,44 @@ cudaError_t plan_group(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) {
   k.m = static_cast<int>(c.m);
   k.cl = c.channels_last ? 1 : 0;
   k.vec = vector_ok ? 1 : 0;
+  k.bcast = c.bcast ? 1 : 0;
+  k.force = force_route;
   if (cache.get(k, p)) return cudaSuccess;
-  e = plan_group_uncached(c, vector_ok, p);
+  e = plan_group_uncached(c, vector_ok, force_route, p);
   if (e == cudaSuccess) cache.put(k, *p);
   return e;
 }
 
-static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) {
+static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, int force,
+                                       GroupPlan* p) {
   *p = GroupPlan{};
+  if (force == 3) {
+    *p = two_phase_plan(c);
+    return cudaSuccess;
+  }
+  if (force == 4) return plan_l2_route(c, vector_ok, p) ? cudaSuccess : cudaErrorNotSupported;
+  if (force == 0 && c.channels_last) {
+    // NHWC: the cooperative route while each of its CTAs merges at most
+    // kCoopMergeMax (partial, group) moments after the barrier; otherwise
+    // the L2 route, whose last CTA per batch item merges once.  (Measured
+    // on GB300: e.g. (2, 64, 64, 320) fp16, 76 x 32 merges: 14.4 us
+    // cooperative vs 16.2 us through L2; (1, 128, 128, 128) fp16,
+    // 152 x 32 merges: 15.6 us vs 11.9 us.)
+    GroupPlan coop;
+    const bool have_coop = plan_group_uncached(c, vector_ok, 2, &coop) == cudaSuccess;
+    if (have_coop && static_cast<int64_t>(coop.ctas_per_item) * c.groups <= kCoopMergeMax) {
+      *p = coop;
+      return cudaSuccess;
+    }
+    if (plan_l2_route(c, vector_ok, p)) return cudaSuccess;
+    if (have_coop) {
+      *p = coop;
+      return cudaSuccess;
+    }
+    *p = two_phase_plan(c);
+    return cudaSuccess;
+  }
+  if (force == 2 && !c.channels_last) return cudaErrorNotSupported;
   const int64_t HW = c.H * c.W;
   const int64_t cpg = c.C / c.groups;
   const int64_t L = cpg * HW;
@@ -251,6 +338,7 @@ static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, G
       return cudaSuccess;
     }
   }
+  if (force == 2) return cudaErrorNotSupported;
   *p = two_phase_plan(c);
   return cudaSuccess;
 }

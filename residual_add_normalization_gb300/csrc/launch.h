@@ -131,13 +131,14 @@ struct GroupPlan {
   int route;      // 1: NCHW resident (CTA / cluster per group instance)
                   // 2: NHWC cooperative (grid barrier)
                   // 3: two-phase partials -> normalize (any shape)
+                  // 4: NHWC through L2 (statistics kernel, then apply kernel)
   int ve;         // elements per vector access, or 1
   int nv;         // vectors held per thread
   int block;      // threads per CTA
   int csize;      // CTAs per cluster (route 1)
   int64_t grid;   // CTAs
-  int ctas_per_item;   // route 2: CTAs per batch item
-  int pix_per_cta;     // route 2: pixels per CTA
+  int ctas_per_item;   // routes 2, 4: CTAs per batch item
+  int pix_per_cta;     // routes 2, 4: pixels per CTA
   int chunks;          // route 3: chunks per group instance
   size_t smem;         // dynamic shared memory bytes
 };
@@ -146,8 +147,10 @@ constexpr size_t kControlBytes = 256;
 constexpr int kTwoPhaseChunk = 4096;   // elements per CTA in route 3
 constexpr int kMaxCoopCtas = 2048;     // upper bound of route-2 grids
 
-size_t group_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int groups);
-cudaError_t plan_group(const SkipGroupCall& c, bool vector_ok, GroupPlan* plan);
+size_t group_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int groups, DType t);
+// force_route 0 picks the route; 2, 3 or 4 asks for that route and returns
+// cudaErrorNotSupported when it cannot take the call.
+cudaError_t plan_group(const SkipGroupCall& c, bool vector_ok, int force_route, GroupPlan* plan);
 GroupPlan two_phase_plan(const SkipGroupCall& c);
 cudaError_t launch_group(const SkipGroupCall& c, const GroupPlan& p, cudaStream_t stream);
 

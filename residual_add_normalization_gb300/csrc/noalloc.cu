@@ -56,7 +56,9 @@ extern "C" B200NORM_API b200norm_status b200norm_skip_group_noalloc(
   // message before anything touches the device.
   char msg[256];
   if (N > 0 && C > 0 && H > 0 && W > 0 && groups > 0 && C % groups == 0) {
-    const size_t need = b200norm::group_workspace_bytes(N, C, H, W, groups);
+    // (the size depends on the element size only)
+    const size_t need = b200norm::group_workspace_bytes(
+        N, C, H, W, groups, T == B200NORM_F32 ? b200norm::DType::F32 : b200norm::DType::F16);
     if (need > kScratchBytes) {
       snprintf(msg, sizeof(msg),
                "this shape needs %zu bytes of scratch, more than the %zu-byte static scratch "

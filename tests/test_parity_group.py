@@ -1,8 +1,9 @@
 """GPU parity: SkipGroupNorm kernels against the CPU oracle on the same seeded
 inputs, through the C ABI (via the binding).
 
-Covers the three routes (NCHW: CTA / cluster per group instance; NHWC: a
-cooperative grid with one bounded grid barrier; two-phase for anything else),
+Covers the four routes (NCHW: CTA / cluster per group instance; NHWC: a
+statistics kernel and an apply kernel through L2, or a cooperative grid with
+one bounded grid barrier; two-phase for anything else),
 both layouts, both T and both M, full / (N, C) / (N, 1, 1, C) skip, bias and S
 on and off, SiLU on and off, vector and scalar paths, and ragged slabs.
 """
@@ -101,6 +102,8 @@ NHWC_CASES = [
     (4, 1, 1, 6, 6),
     (1, 256, 256, 64, 1),   # one 4M-element group
     (2, 64, 64, 96, 24),    # cpg 4: 8-channel vectors span two groups
+    (64, 8, 8, 64, 8),      # 64 batch items: the cooperative route
+    (1, 128, 128, 128, 32), # one item over every SM, 32 groups: the L2 route
 ]
 
 
@@ -125,6 +128,25 @@ def test_forced_two_phase(cl, dtype):
     check(d, 8, 1, cl)
 
 
+@pytest.mark.parametrize("route", [2, 4])
+@pytest.mark.parametrize("dtype,mdtype", TYPE_PAIRS)
+@pytest.mark.parametrize("case", NHWC_CASES)
+def test_nhwc_forced_routes(route, dtype, mdtype, case):
+    """Both NHWC routes on every NHWC case they can take (the planner picks
+    route 4 for tensors that stay in L2 and route 2 for larger ones)."""
+    N, H, W, C, G = case
+    assert b2.library().b200norm_testing_force(0, route) == 0
+    for skip, bias, act, want_sum in (("nc", True, 1, True), ("full", False, 0, False)):
+        d = synthetic.skip_group_inputs((N, H, W, C), dtype, mdtype, seed=N + H + W + C + route,
+                                        channels_last=1, skip=skip, bias=bias, x_std=1.5)
+        try:
+            check(d, G, act, 1, want_sum=want_sum)
+        except b2.B200NormError as e:
+            if "forced route" in str(e):
+                pytest.skip(f"route {route} cannot take {case}: {e}")
+            raise
+
+
 def test_route_coverage():
     routes = set()
     for N, C, H, W, G in NCHW_CASES:
@@ -132,8 +154,12 @@ def test_route_coverage():
         routes.add((p["route"], p["csize"] > 1))
     for N, H, W, C, G in NHWC_CASES:
         routes.add((plan((N, H, W, C), G, np.float16, np.float32, 1)["route"], False))
-    assert {r for r, _ in routes} == {1, 2, 3}
+    assert {r for r, _ in routes} == {1, 2, 3, 4}
     assert (1, True) in routes, "no cluster-per-instance case"
+    # the cooperative route while its per-CTA merge is small, else through L2
+    assert plan((2, 64, 64, 320), 32, np.float16, np.float32, 1)["route"] == 2
+    assert plan((1, 128, 128, 128), 32, np.float16, np.float32, 1)["route"] == 4
+    assert plan((64, 8, 8, 64), 8, np.float16, np.float32, 1)["route"] == 2
 
 
 def test_n11c_at_hw1_equals_nc_route():
