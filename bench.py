@@ -249,7 +249,7 @@ def launches_per_call(b2, spec):
                                              code[np.dtype(spec["dtype"])],
                                              code[np.dtype(spec["mdtype"])],
                                              spec["channels_last"], 1, out)
-    return 2 if out[0] == 3 else 1
+    return 2 if out[0] in (3, 4) else 1
 
 
 def run_ours(args, rank, world, dist):

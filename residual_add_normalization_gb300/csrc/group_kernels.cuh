@@ -147,11 +147,17 @@ __device__ __forceinline__ unsigned fdiv(unsigned n, FastDiv f) {
 // two-pass statistics from there; cluster partial sums meet through DSMEM.
 // VE > 1 needs H*W % VE == 0 so that a vector never straddles two channels;
 // vpc = H*W / VE vectors per channel.
+#ifndef B200NORM_NCHW_UNROLL
+#define B200NORM_NCHW_UNROLL 4   // vectors per thread in flight while loading
+#endif
+#ifndef B200NORM_NCHW_MINB
+#define B200NORM_NCHW_MINB 4     // resident CTAs per SM the registers allow
+#endif
 constexpr int kNchwThreads = 256;
-constexpr int kNchwUnroll = 4;
+constexpr int kNchwUnroll = B200NORM_NCHW_UNROLL;
 
 template <typename T, typename M, int VE>
-__global__ void __launch_bounds__(kNchwThreads, 4)
+__global__ void __launch_bounds__(kNchwThreads, B200NORM_NCHW_MINB)
 sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
   pdl_wait();
   pdl_trigger();

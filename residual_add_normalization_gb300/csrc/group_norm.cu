@@ -170,6 +170,10 @@ static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, i
 
 constexpr int64_t kCoopMergeMax = 3000;
 
+#ifndef B200NORM_NCHW_TARGET_KB
+#define B200NORM_NCHW_TARGET_KB 40  // S staged per CTA in route 1
+#endif
+
 // Plans depend on the device, the shape, the types, the alignment and a
 // forced route only; the occupancy queries behind them are costly, so they
 // are cached.
@@ -250,7 +254,7 @@ static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, i
     const int64_t nvec = L / ve;
     const int64_t vbytes = static_cast<int64_t>(ve) * static_cast<int64_t>(dtype_size(c.t));
     const int64_t insts = c.N * c.groups;
-    const int64_t target = 40 * 1024;
+    const int64_t target = B200NORM_NCHW_TARGET_KB * 1024;
     int64_t cs = cdiv(nvec * vbytes, target);
     while (cs < 16 && insts * cs < 2LL * sms && cdiv(nvec, cs * 2) >= 2LL * kNchwThreads) cs *= 2;
     if (cs > 16 || L > 0x7fffffffLL) {
