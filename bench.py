@@ -50,7 +50,7 @@ FALLBACK_HBM_GBS = 6800.0
 # the current sources).
 NCU_TRAFFIC = {
     # ncu --set full of the GatedRMSNorm lane kernel: 536.9 MB read + 230.7 MB written
-    ("gated_fp16_4x4096x8192_c128", "9f92b667a5565beb"): 767554560,
+    ("gated_fp16_4x4096x8192_c128", "5022fbe461bc86df"): 767554560,
 }
 
 
@@ -194,6 +194,22 @@ def capture(torch, fn, stream):
     return g
 
 
+def max_over_ranks(torch, dist, ms, device):
+    """The largest of every rank's `ms` (the job takes as long as its slowest
+    replica); `ms` itself without a process group."""
+    if not dist:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(step_bytes, world, ms_per_step):
+    """Whole-job throughput: every replica moves `step_bytes` per step, and a
+    step of the job takes `ms_per_step` (the slowest replica's)."""
+    return step_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+
 def op_graphs_of(torch, calls, stream):
     """One graph per workload: 4 x nsets calls cycling through its sets."""
     graphs, reps = [], []
@@ -315,11 +331,7 @@ def run_ours(args, rank, world, dist):
         dist.barrier()
     time.sleep(0.1)
     clocks.stop()
-    total_ms = start.elapsed_time(end)
-    if dist:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(torch, dist, start.elapsed_time(end), dev)
 
     # --- per-operator launch durations (events around each operator graph) --
     op_rounds = max(3, min(50, args.steps // 20))
@@ -428,18 +440,14 @@ def run_ours(args, rank, world, dist):
             stream.wait_stream(st)
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        if dist:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / e2e_steps, dev)
 
     if rank != 0:
         return None
 
     step_bytes = sum(c["bytes"] for c in calls)
     ms_per_step = total_ms / args.steps
-    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    value = job_gbs(step_bytes, world, ms_per_step)
     peak, peak_src = peak_hbm()
     per_op = {c["name"]: op_entry(c, ms) for c, ms in zip(calls, per_call_ms)}
     dom = int(np.argmax(per_call_ms))
@@ -495,9 +503,25 @@ def _workload(name):
     return _WORKLOAD_CACHE[name]
 
 
-def oracle_sample(fraction):
+def _parallel(fn, parts, threads):
+    """Run fn(lo, hi) over `threads` contiguous slices of range(parts) (the C
+    oracle releases the GIL) and return the wall time."""
+    import concurrent.futures as cf
+    k = max(1, min(threads, parts))
+    bounds = [(parts * i // k, parts * (i + 1) // k) for i in range(k)]
+    t0 = time.perf_counter()
+    if k == 1:
+        fn(0, parts)
+    else:
+        with cf.ThreadPoolExecutor(k) as ex:
+            list(ex.map(lambda b: fn(*b), bounds))
+    return time.perf_counter() - t0
+
+
+def oracle_sample(fraction, threads=1):
     """Run the oracle on ``fraction`` of every step workload (leading rows /
-    spans / batch items) and return (algorithmic bytes covered, seconds)."""
+    spans / batch items), split over ``threads`` host threads along that
+    leading axis, and return (algorithmic bytes covered, seconds)."""
     import oracle
     total_bytes, total_s = 0.0, 0.0
     for name in STEP_WORKLOADS:
@@ -506,28 +530,23 @@ def oracle_sample(fraction):
         lead = max(1, int(round(shape[0] * fraction)))
         if spec["op"] == "skip_rms":
             rows = max(1, int(round(np.prod(shape[:-1]) * fraction)))
-            x = d["input"].reshape(-1, shape[-1])[:rows]
-            sk = d["skip"].reshape(-1, shape[-1])[:rows]
-            t0 = time.perf_counter()
-            oracle.skip_rms(x, sk, d["gamma"], d["bias"], epsilon=spec["epsilon"])
-            total_s += time.perf_counter() - t0
+            x = d["input"].reshape(-1, shape[-1])
+            sk = d["skip"].reshape(-1, shape[-1])
+            total_s += _parallel(lambda lo, hi: oracle.skip_rms(
+                x[lo:hi], sk[lo:hi], d["gamma"], d["bias"], epsilon=spec["epsilon"]), rows, threads)
             total_bytes += synthetic.algorithmic_bytes(name) * rows / np.prod(shape[:-1])
         elif spec["op"] == "gated_rms":
             spans = max(1, int(round(np.prod(shape) // spec["C"] * fraction)))
-            x = d["x"].reshape(-1, spec["C"])[:spans]
-            g = d["gate"].reshape(-1, spec["C"])[:spans]
-            t0 = time.perf_counter()
-            oracle.gated_rms(x, g, d["scale"], epsilon=spec["epsilon"])
-            total_s += time.perf_counter() - t0
+            x = d["x"].reshape(-1, spec["C"])
+            g = d["gate"].reshape(-1, spec["C"])
+            total_s += _parallel(lambda lo, hi: oracle.gated_rms(
+                x[lo:hi], g[lo:hi], d["scale"], epsilon=spec["epsilon"]), spans, threads)
             total_bytes += synthetic.algorithmic_bytes(name) * spans / (np.prod(shape) // spec["C"])
         else:
-            x = d["x"][:lead]
-            sk = d["skip"][:lead]
-            t0 = time.perf_counter()
-            oracle.skip_group(x, sk, d["gamma"], d["beta"], d["bias"], groups=spec["groups"],
-                              activation=spec["activation"], epsilon=spec["epsilon"],
-                              channels_last=spec["channels_last"], want_sum=spec["want_sum"])
-            total_s += time.perf_counter() - t0
+            total_s += _parallel(lambda lo, hi: oracle.skip_group(
+                d["x"][lo:hi], d["skip"][lo:hi], d["gamma"], d["beta"], d["bias"],
+                groups=spec["groups"], activation=spec["activation"], epsilon=spec["epsilon"],
+                channels_last=spec["channels_last"], want_sum=spec["want_sum"]), lead, threads)
             total_bytes += synthetic.algorithmic_bytes(name) * lead / shape[0]
     return total_bytes, total_s
 
@@ -539,6 +558,16 @@ def cpu_baseline(budget_s=15.0):
     return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"leading {frac:.4f} of the rows / C-spans / batch items of each step "
                       f"workload, single-threaded C oracle ({s:.1f} s)"}
+
+
+def cpu_baseline_all_cores():
+    """The same oracle partitioned over every host core this process may use
+    (rows, spans, or batch items; the results do not depend on the split)."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    b, s = oracle_sample(1.0, threads=cores)
+    return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"every step workload, split over {cores} threads along the leading axis "
+                      f"(SkipGroupNorm by batch item: 2 and 16 items) ({s:.1f} s)"}
 
 
 def run_reference(args):
@@ -610,6 +639,7 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()
+            line["cpu_baseline_all_cores"] = cpu_baseline_all_cores()
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

@@ -47,7 +47,9 @@ def _inputs_digest() -> str:
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
-    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    # flags without the include paths, so the digest does not depend on where
+    # the tree sits
+    h.update(" ".join(ARCH + [f for f in NVCC_FLAGS if not f.startswith("-I")]).encode())
     return h.hexdigest()
 
 

@@ -200,3 +200,30 @@ def test_empty_batch():
     y, s = b2.skip_group(x, torch.empty((0, 8), dtype=torch.float16, device="cuda"), g, g,
                          groups=2, activation=0)
     assert y.shape == x.shape
+
+
+def test_one_workspace_serves_every_route_in_turn():
+    """One explicit workspace, calls of different shapes and routes in turn
+    (the L2 route's per-item counters and the cooperative route's barrier live
+    in its control block; partial slots are overwritten by every route)."""
+    calls = [((2, 64, 64, 320), 1, 32, None), ((1, 128, 128, 128), 1, 32, None),
+             ((5, 16, 16, 64), 1, 8, 4), ((2, 64, 16, 16), 0, 8, None),
+             ((1, 128, 128, 128), 1, 32, None), ((3, 16, 16, 96), 1, 12, 3),
+             ((2, 64, 64, 320), 1, 32, 4), ((64, 8, 8, 64), 1, 8, None)]
+    need = max(b2.workspace_size(*(s[0], s[3], s[1], s[2]) if cl else s, g, torch.float16, cl)
+               for s, cl, g, _ in calls)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    lib = b2.library()
+    for i, (shape, cl, G, force) in enumerate(calls):
+        assert lib.b200norm_testing_force(0, force or 0) == 0
+        d = synthetic.skip_group_inputs(shape, np.float16, np.float32, seed=40 + i,
+                                        channels_last=cl, skip="nc", bias=True)
+        y, s = b2.skip_group(to_dev(d["x"]), to_dev(d["skip"]), to_dev(d["gamma"]),
+                             to_dev(d["beta"]), to_dev(d["bias"]), groups=G, activation=1,
+                             channels_last=cl, want_sum=True, workspace=ws)
+        torch.cuda.synchronize()
+        ry, rs = oracle.skip_group(d["x"], d["skip"], d["gamma"], d["beta"], d["bias"], groups=G,
+                                   activation=1, channels_last=cl)
+        assert_bitexact(to_host(s), rs)
+        assert_y_close(to_host(y), ry)
+    b2.workspace_status(ws)
