@@ -217,6 +217,24 @@ __device__ __forceinline__ float cta_sum(float v, float* red) {
   return red[32];
 }
 
+// Two CTA-wide sums at once (one pair of barriers); `red` holds 33 float2.
+__device__ __forceinline__ float2 cta_sum2(float2 v, float2* red) {
+  v.x = warp_sum(v.x);
+  v.y = warp_sum(v.y);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    float2 t = lane < nwarps ? red[lane] : make_float2(0.0f, 0.0f);
+    t.x = warp_sum(t.x);
+    t.y = warp_sum(t.y);
+    if (lane == 0) red[32] = t;
+  }
+  __syncthreads();
+  return red[32];
+}
+
 // ---------------------------------------------------------------------------
 // Thread-block clusters (distributed shared memory)
 // ---------------------------------------------------------------------------
@@ -259,6 +277,22 @@ __device__ __forceinline__ float cluster_sum(float cta_value, float* slot, unsig
   cluster_sync();
   float t = 0.0f;
   for (unsigned r = 0; r < csize; ++r) t += ld_cluster_f32(slot, r);
+  return t;
+}
+
+// Two values per CTA summed over the cluster at once (one cluster barrier).
+__device__ __forceinline__ float2 cluster_sum2(float2 cta_value, float* slot_x, float* slot_y,
+                                               unsigned csize) {
+  if (threadIdx.x == 0) {
+    *slot_x = cta_value.x;
+    *slot_y = cta_value.y;
+  }
+  cluster_sync();
+  float2 t = make_float2(0.0f, 0.0f);
+  for (unsigned r = 0; r < csize; ++r) {
+    t.x += ld_cluster_f32(slot_x, r);
+    t.y += ld_cluster_f32(slot_y, r);
+  }
   return t;
 }
 

@@ -10,15 +10,14 @@
 //   1. NCHW resident.  A group instance (n, g) is one contiguous run of
 //      cpg * H * W elements.  One CTA -- or a cluster of up to 16 CTAs for
 //      long runs -- stages its share of S in shared memory: one HBM read,
-//      exact two-pass (centred) statistics from shared memory, one write.
+//      statistics from shifted sums taken while loading, one write.
 //      Cluster partials are exchanged through distributed shared memory.
 //   2. NHWC cooperative.  A group's elements are strided through the tensor
 //      (cpg channels of every pixel), so statistics need every CTA that holds
 //      a piece of the batch item.  One cooperative grid: each CTA holds a
-//      slab of whole pixels in registers, takes its slab's per-group
-//      (count, mean, M2) with two passes of plain additions, publishes them,
-//      meets the other CTAs at one bounded grid barrier, merges its batch
-//      item's partials with Chan's formula and normalizes what it holds.
+//      slab of whole pixels in registers, takes its slab's per-group shifted
+//      sums, publishes them, meets the other CTAs at one bounded grid
+//      barrier, adds its batch item's partials and normalizes what it holds.
 //   3. Two-phase, any shape or layout.  Kernel A forms S over fixed chunks of
 //      each group instance and writes per-chunk moments; kernel B merges them
 //      and re-forms S from the inputs to normalize (the re-read is an L2 hit
@@ -143,8 +142,9 @@ __device__ __forceinline__ unsigned fdiv(unsigned n, FastDiv f) {
 // A group instance (n, g) is the contiguous run of L = cpg * H * W elements at
 // (n*C + g*cpg) * H*W.  CTA rank r of the instance's cluster takes vectors
 // [r * span, (r + 1) * span) of it: it loads X (+ skip), forms S, keeps S in
-// shared memory (span vectors of dynamic shared memory), and takes exact
-// two-pass statistics from there; cluster partial sums meet through DSMEM.
+// shared memory (span vectors of dynamic shared memory) and accumulates the
+// sums of S - K and (S - K)^2 on the way (K the instance's first residual sum,
+// so the shifted sums do not cancel); cluster partial sums meet through DSMEM.
 // VE > 1 needs H*W % VE == 0 so that a vector never straddles two channels;
 // vpc = H*W / VE vectors per channel.
 #ifndef B200NORM_NCHW_UNROLL
@@ -164,7 +164,7 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
   using P = Pack<T, VE>;
   extern __shared__ float4 smem4[];
   P* sb = reinterpret_cast<P*>(smem4);
-  __shared__ float red[33];
+  __shared__ float2 red2[33];
   __shared__ float slot_sum, slot_m2;
   const unsigned csize = cluster_size();
   const unsigned rank = csize > 1 ? cluster_rank() : 0u;
@@ -178,7 +178,7 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
   const int cbase = g * a.cpg;
 
   const float K = sgn_shift(a, n, g, false);
-  float sum = 0.0f;
+  float sum = 0.0f, sq = 0.0f;
   for (int i0 = threadIdx.x; i0 < cnt; i0 += kNchwThreads * kNchwUnroll) {
     P xv[kNchwUnroll], kv[kNchwUnroll];
 #pragma unroll
@@ -200,28 +200,23 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
         for (int e = 0; e < VE; ++e) {
           const float sk = a.bcast ? skb : to_f32(kv[u].v[e]);
           sv.v[e] = sgn_sum<T>(to_f32(xv[u].v[e]), sk, a.bias, c);
-          sum += to_f32(sv.v[e]) - K;
+          const float d = to_f32(sv.v[e]) - K;
+          sum += d;
+          sq = fmaf(d, d, sq);
         }
         sb[i] = sv;
         if (a.s) st_stream<T, VE>(a.s + base + static_cast<int64_t>(i) * VE, sv);
       }
     }
   }
-  float tot = cta_sum(sum, red);
-  if (csize > 1) tot = cluster_sum(tot, &slot_sum, csize);
-  const float dmean = tot / static_cast<float>(L);  // mean = K + dmean
-  float m2 = 0.0f;
-  for (int i = threadIdx.x; i < cnt; i += kNchwThreads) {
-    const P sv = sb[i];
-#pragma unroll
-    for (int e = 0; e < VE; ++e) {
-      const float d = (to_f32(sv.v[e]) - K) - dmean;
-      m2 = fmaf(d, d, m2);
-    }
-  }
-  tot = cta_sum(m2, red);
-  if (csize > 1) tot = cluster_sum(tot, &slot_m2, csize);
-  const float rstd = 1.0f / sqrtf(tot / static_cast<float>(L) + a.eps);
+  // one pass of shifted sums: mean = K + dmean, var = E[(S-K)^2] - dmean^2
+  // (K is a value of the group, so |dmean| is of the order of its spread)
+  float2 t2 = cta_sum2(make_float2(sum, sq), red2);
+  if (csize > 1) t2 = cluster_sum2(t2, &slot_sum, &slot_m2, csize);
+  const float tot = t2.x, tsq = t2.y;
+  const float dmean = tot / static_cast<float>(L);
+  const float var = fmaxf(tsq / static_cast<float>(L) - dmean * dmean, 0.0f);
+  const float rstd = 1.0f / sqrtf(var + a.eps);
   for (int i = threadIdx.x; i < cnt; i += kNchwThreads) {
     const int c = cbase + static_cast<int>(fdiv(static_cast<unsigned>(v0 + i), vpc));
     const float ga = to_f32(a.gamma[c]), be = to_f32(a.beta[c]);
@@ -241,13 +236,15 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
 // blockDim.x = CV * PL with CV = C / VE vectors per pixel: thread t covers the
 // VE channels (t % CV) * VE .. +VE of pixels p0 + t / CV + k * PL, k < NV.
 // CTA b handles batch item b / B, pixels [(b % B) * ppc, +ppc).
-// Inside a CTA the statistics are an exact two-pass over the held S (sums
-// only: per thread, per pixel lane and channel, then per group); across CTAs
-// the (count, mean, M2) partials meet with Chan's merge after one grid
-// barrier.  All moments are of S - K[g], K[g] the group's first residual sum.
+// Every CTA takes, per group, the count and the sums of S - K[g] and
+// (S - K[g])^2 over the S it holds (K[g] the group's first residual sum, the
+// same in every CTA, so the shifted sums do not cancel): per thread, per
+// pixel lane and channel, then per group.  After one grid barrier each CTA adds
+// its batch item's partials in a fixed order: mean = K + d,
+// var = sum((S - K)^2) / n - d^2.
 // Dynamic shared memory (floats), layout given by k_offset:
-//   passes:  acc[PL*C] | col[C] | gmean[groups]
-//   merge:   chunk moments[nchunk*groups*3] | gmean[groups] | grstd[groups]
+//   sums:    acc[2][PL*C] | col[2][C]
+//   merge:   chunk sums[nchunk*groups*3] | mean offset d[groups] | rstd[groups]
 //   tail at k_offset, kept throughout: K[groups] | gamma[C] | beta[C]
 constexpr int kCoopMergeChunk = 4;
 
@@ -296,9 +293,9 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
   float Kl[VE];
 #pragma unroll
   for (int e = 0; e < VE; ++e) Kl[e] = s_K[(c0 + e) / a.cpg];
-  float lsum[VE];
+  float lsum[VE], lsq[VE];
 #pragma unroll
-  for (int e = 0; e < VE; ++e) lsum[e] = 0.0f;
+  for (int e = 0; e < VE; ++e) lsum[e] = lsq[e] = 0.0f;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int p = p0 + tp + k * PL;
@@ -307,69 +304,51 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
       for (int e = 0; e < VE; ++e) {
         const float sk = a.bcast ? to_f32(skb.v[e]) : to_f32(kv[k].v[e]);
         sv[k].v[e] = sgn_sum_b<T>(to_f32(xv[k].v[e]), sk, to_f32(bv.v[e]), a.bias != nullptr);
-        lsum[e] += to_f32(sv[k].v[e]) - Kl[e];
+        const float d = to_f32(sv[k].v[e]) - Kl[e];
+        lsum[e] += d;
+        lsq[e] = fmaf(d, d, lsq[e]);
       }
     }
   }
-  // acc is laid out [e][tp][tc] so that the stores of a warp hit distinct banks
+  // --- CTA sums of S - K and (S - K)^2 per group ---------------------------
+  // acc is laid out [q][e][tp][tc] so that the stores of a warp hit distinct
+  // banks; col is [q][C]
   float* s_acc = smem;
-  float* s_col = smem + PL * C;
-  float* s_gm = s_col + C;
-  const float n_cta = static_cast<float>(p1 - p0) * static_cast<float>(a.cpg);
-
-  // --- pass 1: CTA-local group means of S - K ----------------------------
-#pragma unroll
-  for (int e = 0; e < VE; ++e) s_acc[(e * PL + tp) * CV + tc] = lsum[e];
-  __syncthreads();
-  for (int j = threadIdx.x; j < C; j += blockDim.x) {
-    const int e = j / CV, q0 = j % CV;
-    float t = 0.0f;
-    for (int q = 0; q < PL; ++q) t += s_acc[(e * PL + q) * CV + q0];
-    s_col[q0 * VE + e] = t;
-  }
-  __syncthreads();
-  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
-    float t = 0.0f;
-    for (int cc = 0; cc < a.cpg; ++cc) t += s_col[gg * a.cpg + cc];
-    s_gm[gg] = t / n_cta;
-  }
-  __syncthreads();
-  // --- pass 2: CTA-local sums of squared deviations ----------------------
-  float gml[VE];
-#pragma unroll
-  for (int e = 0; e < VE; ++e) gml[e] = s_gm[(c0 + e) / a.cpg];
+  float* s_col = smem + 2 * PL * C;
+  const int nthr = PL * CV;
 #pragma unroll
   for (int e = 0; e < VE; ++e) {
-    float m2 = 0.0f;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      const int p = p0 + tp + k * PL;
-      if (p < p1) {
-        const float d = (to_f32(sv[k].v[e]) - Kl[e]) - gml[e];
-        m2 = fmaf(d, d, m2);
-      }
-    }
-    s_acc[(e * PL + tp) * CV + tc] = m2;
+    s_acc[(e * PL + tp) * CV + tc] = lsum[e];
+    s_acc[nthr * VE + (e * PL + tp) * CV + tc] = lsq[e];
   }
   __syncthreads();
   for (int j = threadIdx.x; j < C; j += blockDim.x) {
     const int e = j / CV, q0 = j % CV;
-    float t = 0.0f;
-    for (int q = 0; q < PL; ++q) t += s_acc[(e * PL + q) * CV + q0];
-    s_col[q0 * VE + e] = t;
+    float t1 = 0.0f, t2 = 0.0f;
+    for (int q = 0; q < PL; ++q) {
+      t1 += s_acc[(e * PL + q) * CV + q0];
+      t2 += s_acc[nthr * VE + (e * PL + q) * CV + q0];
+    }
+    s_col[q0 * VE + e] = t1;
+    s_col[C + q0 * VE + e] = t2;
   }
   __syncthreads();
+  const float n_cta = static_cast<float>(p1 - p0) * static_cast<float>(a.cpg);
   for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
-    float t = 0.0f;
-    for (int cc = 0; cc < a.cpg; ++cc) t += s_col[gg * a.cpg + cc];
-    a.part[static_cast<int64_t>(blockIdx.x) * a.groups + gg] = make_float4(n_cta, s_gm[gg], t, 0.0f);
+    float t1 = 0.0f, t2 = 0.0f;
+    for (int cc = 0; cc < a.cpg; ++cc) {
+      t1 += s_col[gg * a.cpg + cc];
+      t2 += s_col[C + gg * a.cpg + cc];
+    }
+    a.part[static_cast<int64_t>(blockIdx.x) * a.groups + gg] = make_float4(n_cta, t1, t2, 0.0f);
   }
   __threadfence();  // partials visible GPU-wide before this CTA arrives
   if (!grid_barrier(a.ctl, gridDim.x, a.limit_ns, 1u)) return;
 
-  // --- merge the batch item's B partials per group ------------------------
+  // --- add the batch item's B partials per group (every CTA shifts by the
+  // same K, so plain sums in a fixed order) -----------------------------------
   // chunks of kCoopMergeChunk partials: all loads of a chunk are issued
-  // before its merges, then the chunk results are merged per group
+  // before they are added, then the chunk sums are added per group
   const int nchunk = (B + kCoopMergeChunk - 1) / kCoopMergeChunk;
   float* s_cm = smem;                                  // nchunk * groups * 3
   float* s_gmean = smem + nchunk * a.groups * 3;
@@ -382,23 +361,30 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
 #pragma unroll
     for (int j = 0; j < kCoopMergeChunk; ++j)
       if (b0 + j < B) u[j] = __ldcg(src + static_cast<int64_t>(b0 + j) * a.groups + gg);
-    Moments m{0.0f, 0.0f, 0.0f};
+    float cn = 0.0f, c1 = 0.0f, c2 = 0.0f;
 #pragma unroll
     for (int j = 0; j < kCoopMergeChunk; ++j)
-      if (b0 + j < B) m = merge(m, Moments{u[j].x, u[j].y, u[j].z});
-    s_cm[idx * 3] = m.n;
-    s_cm[idx * 3 + 1] = m.mean;
-    s_cm[idx * 3 + 2] = m.m2;
+      if (b0 + j < B) {
+        cn += u[j].x;
+        c1 += u[j].y;
+        c2 += u[j].z;
+      }
+    s_cm[idx * 3] = cn;
+    s_cm[idx * 3 + 1] = c1;
+    s_cm[idx * 3 + 2] = c2;
   }
   __syncthreads();
   for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
-    Moments m{0.0f, 0.0f, 0.0f};
+    float cn = 0.0f, c1 = 0.0f, c2 = 0.0f;
     for (int q = 0; q < nchunk; ++q) {
       const int idx = q * a.groups + gg;
-      m = merge(m, Moments{s_cm[idx * 3], s_cm[idx * 3 + 1], s_cm[idx * 3 + 2]});
+      cn += s_cm[idx * 3];
+      c1 += s_cm[idx * 3 + 1];
+      c2 += s_cm[idx * 3 + 2];
     }
-    s_gmean[gg] = m.mean;
-    s_grstd[gg] = 1.0f / sqrtf(m.m2 / m.n + a.eps);
+    const float d = c1 / cn;
+    s_gmean[gg] = d;
+    s_grstd[gg] = 1.0f / sqrtf(fmaxf(c2 / cn - d * d, 0.0f) + a.eps);
   }
   __syncthreads();
   // --- normalize what this thread holds; store S and Y ---------------------
@@ -823,7 +809,7 @@ sgn_normalize(const SgnArgs<T, M> a, int chunks) {
 // Kernel selection and typed launch (host)
 // ---------------------------------------------------------------------------
 inline size_t coop_k_offset(int PL, int C, int B, int groups) {
-  const size_t passes = static_cast<size_t>(PL) * C + C + groups;
+  const size_t passes = 2 * (static_cast<size_t>(PL) * C + C);
   const size_t nchunk = (static_cast<size_t>(B) + kCoopMergeChunk - 1) / kCoopMergeChunk;
   const size_t merge = nchunk * groups * 3 + 2ull * groups;
   const size_t off = passes > merge ? passes : merge;

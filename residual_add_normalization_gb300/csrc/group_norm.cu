@@ -168,7 +168,6 @@ static bool plan_l2_route(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) 
 static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, int force,
                                        GroupPlan* p);
 
-constexpr int64_t kCoopMergeMax = 3000;
 
 #ifndef B200NORM_NCHW_TARGET_KB
 #define B200NORM_NCHW_TARGET_KB 40  // S staged per CTA in route 1
@@ -215,23 +214,12 @@ static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, i
   }
   if (force == 4) return plan_l2_route(c, vector_ok, p) ? cudaSuccess : cudaErrorNotSupported;
   if (force == 0 && c.channels_last) {
-    // NHWC: the cooperative route while each of its CTAs merges at most
-    // kCoopMergeMax (partial, group) moments after the barrier; otherwise
-    // the L2 route, whose last CTA per batch item merges once.  (Measured
-    // on GB300: e.g. (2, 64, 64, 320) fp16, 76 x 32 merges: 14.4 us
-    // cooperative vs 16.2 us through L2; (1, 128, 128, 128) fp16,
-    // 152 x 32 merges: 15.6 us vs 11.9 us.)
-    GroupPlan coop;
-    const bool have_coop = plan_group_uncached(c, vector_ok, 2, &coop) == cudaSuccess;
-    if (have_coop && static_cast<int64_t>(coop.ctas_per_item) * c.groups <= kCoopMergeMax) {
-      *p = coop;
-      return cudaSuccess;
-    }
+    // NHWC: the cooperative route whenever its grid can be resident, else the
+    // L2 route, else two-phase.  (Measured on GB300: (2, 64, 64, 320) fp16
+    // 11.6 us cooperative vs 16.2 us through L2; (1, 128, 128, 128) fp16
+    // 11.3 vs 11.9 us; (8, 32, 32, 512) fp16 13.5 vs 16.4 us.)
+    if (plan_group_uncached(c, vector_ok, 2, p) == cudaSuccess) return cudaSuccess;
     if (plan_l2_route(c, vector_ok, p)) return cudaSuccess;
-    if (have_coop) {
-      *p = coop;
-      return cudaSuccess;
-    }
     *p = two_phase_plan(c);
     return cudaSuccess;
   }

@@ -103,7 +103,7 @@ NHWC_CASES = [
     (1, 256, 256, 64, 1),   # one 4M-element group
     (2, 64, 64, 96, 24),    # cpg 4: 8-channel vectors span two groups
     (64, 8, 8, 64, 8),      # 64 batch items: the cooperative route
-    (1, 128, 128, 128, 32), # one item over every SM, 32 groups: the L2 route
+    (1, 128, 128, 128, 32), # one item over every SM, 32 groups
 ]
 
 
@@ -154,12 +154,12 @@ def test_route_coverage():
         routes.add((p["route"], p["csize"] > 1))
     for N, H, W, C, G in NHWC_CASES:
         routes.add((plan((N, H, W, C), G, np.float16, np.float32, 1)["route"], False))
-    assert {r for r, _ in routes} == {1, 2, 3, 4}
+    assert {r for r, _ in routes} == {1, 2, 3}
     assert (1, True) in routes, "no cluster-per-instance case"
-    # the cooperative route while its per-CTA merge is small, else through L2
+    # the cooperative route while its grid can be resident, else through L2
     assert plan((2, 64, 64, 320), 32, np.float16, np.float32, 1)["route"] == 2
-    assert plan((1, 128, 128, 128), 32, np.float16, np.float32, 1)["route"] == 4
     assert plan((64, 8, 8, 64), 8, np.float16, np.float32, 1)["route"] == 2
+    assert plan((4, 64, 64, 320), 32, np.float16, np.float32, 1)["route"] == 4
 
 
 def test_n11c_at_hw1_equals_nc_route():
