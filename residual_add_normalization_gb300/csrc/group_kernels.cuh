@@ -148,7 +148,7 @@ __device__ __forceinline__ unsigned fdiv(unsigned n, FastDiv f) {
 // VE > 1 needs H*W % VE == 0 so that a vector never straddles two channels;
 // vpc = H*W / VE vectors per channel.
 #ifndef B200NORM_NCHW_UNROLL
-#define B200NORM_NCHW_UNROLL 4   // vectors per thread in flight while loading
+#define B200NORM_NCHW_UNROLL 2   // vectors per thread in flight while loading (measured)
 #endif
 #ifndef B200NORM_NCHW_MINB
 #define B200NORM_NCHW_MINB 4     // resident CTAs per SM the registers allow
