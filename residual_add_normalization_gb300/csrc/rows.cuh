@@ -226,31 +226,36 @@ struct GatedOp {
 // ---------------------------------------------------------------------------
 constexpr int kRowsMaxThreads = 512;
 
-constexpr int kLaneBlock = 256;     // threads per CTA of the lane-group schedule
-#ifndef B200NORM_LANE_MIN_BLOCKS
-#define B200NORM_LANE_MIN_BLOCKS 8
+// Threads per CTA of the lane-group schedule, by the vectors each thread
+// holds in flight (NV * RPG): 1024 with one (measured about 1% faster than
+// 256 on C = 128 spans), 256 with more, so those keep their registers.
+#ifndef B200NORM_LANE_BLOCK
+#define B200NORM_LANE_BLOCK 1024
 #endif
-// Resident CTAs per SM the lane-group kernel is compiled for: fewer when each
-// thread holds more vectors in flight (NV * RPG), so those keep their registers.
-constexpr int lane_min_blocks(int held) {
-  return B200NORM_LANE_MIN_BLOCKS / held > 0 ? B200NORM_LANE_MIN_BLOCKS / held : 1;
+__host__ __device__ constexpr int lane_block(int held) {
+  return held == 1 ? B200NORM_LANE_BLOCK : 256;
+}
+// Resident CTAs per SM the lane-group kernel is compiled for: a full SM of
+// 2048 threads at one vector per thread, fewer with more vectors in flight.
+__host__ __device__ constexpr int lane_min_blocks(int held) {
+  return 2048 / lane_block(held) / held > 0 ? 2048 / lane_block(held) / held : 1;
 }
 
 // Lane-group schedule (tpr <= 32 threads per row, a power of two).  The grid
 // is persistent: CTA b takes row blocks b, b + gridDim.x, ... of
-// (kLaneBlock / tpr) * RPG rows each; lane group g of the CTA takes rows
-// g + i * (kLaneBlock / tpr), i < RPG, of a block, so each step covers
+// (blockDim.x / tpr) * RPG rows each; lane group g of the CTA takes rows
+// g + i * (blockDim.x / tpr), i < RPG, of a block, so each step covers
 // consecutive rows.  Per-vector weights stay in registers across blocks.
 // nvec: vectors of Op::kVE elements per row, nvec <= NV * tpr.
 template <class Op, int NV, int RPG>
-__global__ void __launch_bounds__(kLaneBlock, lane_min_blocks(NV * RPG))
+__global__ void __launch_bounds__(lane_block(NV * RPG), lane_min_blocks(NV * RPG))
 rows_lane_kernel(const typename Op::Args a, int tpr, int nvec) {
   pdl_wait();
   pdl_trigger();
   typename Op::Wt w[NV];
   const int lane = threadIdx.x & (tpr - 1);
   const int group = threadIdx.x / tpr;
-  const int groups_per_cta = kLaneBlock / tpr;
+  const int groups_per_cta = lane_block(NV * RPG) / tpr;
   const int64_t rows_per_block = static_cast<int64_t>(groups_per_cta) * RPG;
   const int64_t nblocks = (a.rows + rows_per_block - 1) / rows_per_block;
 #pragma unroll

@@ -41,14 +41,14 @@ RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok) {
     p.nv = nvec >= B200NORM_SHORT_NV ? B200NORM_SHORT_NV : 1;
     p.tpr = pow2_ceil(ceil_div(nvec, p.nv));
     p.rpg = p.nv == 1 && p.tpr <= 16 ? B200NORM_SHORT_RPG : 1;
-    p.block = kLaneBlock;
+    p.block = lane_block(p.nv * p.rpg);
     p.grid = ceil_div(rows, static_cast<int64_t>(p.block / p.tpr) * p.rpg);
   } else if (nvec <= 128) {
     // Warp per row, up to four vectors per lane.
     p.mode = 0;
     p.tpr = 32;
     p.nv = pow2_ceil(ceil_div(nvec, 32));
-    p.block = kLaneBlock;
+    p.block = lane_block(p.nv);
     p.grid = ceil_div(rows, p.block / 32);
   } else {
     // CTA per row; a cluster per row once one CTA cannot hold it.

@@ -83,12 +83,12 @@ cudaError_t launch_rows_op(const typename Op::Args& a, const RowPlan& p, cudaStr
   if (p.mode == 0) {
     // persistent lane-group schedule: as many CTAs as can be resident
     int64_t resident = 0;
-    cudaError_t e = resident_ctas(reinterpret_cast<const void*>(fn), kLaneBlock, &resident);
+    cudaError_t e = resident_ctas(reinterpret_cast<const void*>(fn), p.block, &resident);
     if (e != cudaSuccess) return e;
     if (grid > resident) grid = resident;
   }
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(p.mode == 0 ? kLaneBlock : p.block);
+  cfg.blockDim = dim3(p.block);
   cfg.dynamicSmemBytes = 0;
   unsigned nattr = 0;
   if (p.mode == 1 && p.csize > 1) {

@@ -188,7 +188,7 @@ def test_row_planner_shapes(lib):
                 assert n % p["ve"] == 0
                 if p["mode"] != 2:
                     assert p["tpr"] * p["nv"] >= nvec, (n, T, al, p)
-                    assert p["block"] <= 512 and p["block"] % 32 == 0
+                    assert p["block"] <= 1024 and p["block"] % 32 == 0
                 if p["mode"] == 0:
                     assert p["tpr"] & (p["tpr"] - 1) == 0 and p["block"] % p["tpr"] == 0
 
