@@ -79,6 +79,8 @@ def library() -> ctypes.CDLL:
             "b200norm_workspace_status": ([vp, vp], i32),
             "b200norm_testing_barrier_timeout": ([vp, sz, ctypes.c_uint64, vp], i32),
             "b200norm_testing_force": ([i32, i32], i32),
+            "b200norm_testing_force_split": ([i32, i32], i32),
+            "b200norm_testing_set_pdl": ([i32], i32),
             "b200norm_testing_plan_rows": ([i64, i64, i32, i32, ctypes.POINTER(ctypes.c_int64)],
                                            i32),
             "b200norm_testing_plan_group": ([i64, i64, i64, i64, i32, i32, i32, i32, i32,
