@@ -356,6 +356,17 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -369,16 +380,16 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
 __device__ __forceinline__ bool grid_barrier(Control* ctl, unsigned expected,
                                              unsigned long long limit_ns, unsigned site) {
   __shared__ int ok;
-  __syncthreads();
+  __syncthreads();  // every thread's earlier writes are ordered before thread 0's release
   if (threadIdx.x == 0) {
     const unsigned gen = ld_acquire_gpu(&ctl->bar_gen);
-    __threadfence();
-    const unsigned arrived = atomicAdd(&ctl->bar_count, 1u) + 1u;
+    // arrive: release publishes this CTA's writes, acquire (for the last
+    // arrival) sees every other CTA's
+    const unsigned arrived = atom_add_acq_rel_gpu(&ctl->bar_count, 1u) + 1u;
     ok = 1;
     if (arrived == expected) {
-      atomicExch(&ctl->bar_count, 0u);
-      __threadfence();
-      atomicAdd(&ctl->bar_gen, 1u);
+      ctl->bar_count = 0u;                      // ordered before the release below
+      st_release_gpu(&ctl->bar_gen, gen + 1u);  // opens the barrier
     } else {
       const unsigned long long t0 = global_ns();
       while (ld_acquire_gpu(&ctl->bar_gen) == gen) {
@@ -388,10 +399,8 @@ __device__ __forceinline__ bool grid_barrier(Control* ctl, unsigned expected,
           ok = 0;
           break;
         }
-        __nanosleep(64);
       }
     }
-    __threadfence();
   }
   __syncthreads();
   return ok != 0;

@@ -246,7 +246,7 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
 //   sums:    acc[2][PL*C] | col[2][C]
 //   merge:   chunk sums[nchunk*groups*3] | mean offset d[groups] | rstd[groups]
 //   tail at k_offset, kept throughout: K[groups] | gamma[C] | beta[C]
-constexpr int kCoopMergeChunk = 4;
+constexpr int kCoopMergeChunk = 8;
 
 template <typename T, typename M, int VE, int NV>
 __global__ void __launch_bounds__(kCoopMaxThreads, 1)
@@ -342,7 +342,7 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
     }
     a.part[static_cast<int64_t>(blockIdx.x) * a.groups + gg] = make_float4(n_cta, t1, t2, 0.0f);
   }
-  __threadfence();  // partials visible GPU-wide before this CTA arrives
+  // the barrier's release (after a CTA barrier) publishes these partials
   if (!grid_barrier(a.ctl, gridDim.x, a.limit_ns, 1u)) return;
 
   // --- add the batch item's B partials per group (every CTA shifts by the
