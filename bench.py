@@ -46,8 +46,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by
-# the digest of the kernel sources it was taken on (None: not captured for
-# the current sources).
+# the digest of its kernel family's sources when it was taken (None: not
+# captured for the current sources).
 NCU_TRAFFIC = {
     # ncu --set full of the GatedRMSNorm lane kernel: 536.9 MB read + 230.4 MB written
     ("gated_fp16_4x4096x8192_c128", "32f0c61c34e4ae4e"): 767324928,
@@ -454,7 +454,8 @@ def run_ours(args, rank, world, dist):
     dom_c = calls[dom]
     achieved = dom_c["bytes"] / (per_call_ms[dom] * 1e-3) / 1e9
     digest = buildlib.source_digest()
-    traffic = NCU_TRAFFIC.get((dom_c["name"], digest))
+    family = "group" if dom_c["spec"]["op"] == "skip_group" else "rows"
+    traffic = NCU_TRAFFIC.get((dom_c["name"], buildlib.source_digest(family)))
     launches = sum(launches_per_call(b2, c["spec"]) for c in calls) * args.steps
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,

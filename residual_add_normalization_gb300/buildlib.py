@@ -39,10 +39,23 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _inputs_digest() -> str:
+# The sources each kernel family is built from (for digests that identify one
+# family's code, e.g. to key profiler counters taken on it).
+FAMILY_SOURCES = {
+    "rows": ("common.cuh", "launch.h", "rows.cuh", "rows_launch.cuh", "rows_ops.cuh",
+             "rows_gated.cu", "rows_ssln_f16.cu", "rows_ssln_f32.cu", "rows_bf16.cu"),
+    "group": ("common.cuh", "launch.h", "group_kernels.cuh", "group_norm.cu", "group_f32.cu",
+              "group_f16.cu", "group_bf16.cu"),
+}
+
+
+def _inputs_digest(family: str | None = None) -> str:
     h = hashlib.sha256()
-    files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC))
-    files += sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE))
+    if family is None:
+        files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC))
+        files += sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE))
+    else:
+        files = [os.path.join(CSRC, f) for f in FAMILY_SOURCES[family]]
     for f in files:
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
@@ -53,9 +66,10 @@ def _inputs_digest() -> str:
     return h.hexdigest()
 
 
-def source_digest() -> str:
-    """Digest of the kernel sources and headers (identifies a kernel build)."""
-    return _inputs_digest()[:16]
+def source_digest(family: str | None = None) -> str:
+    """Digest of the kernel sources and headers (identifies a kernel build), or
+    of one kernel family's sources ("rows", "group")."""
+    return _inputs_digest(family)[:16]
 
 
 def _compile(src: str) -> str:

@@ -153,7 +153,10 @@ __device__ __forceinline__ unsigned fdiv(unsigned n, FastDiv f) {
 #ifndef B200NORM_NCHW_MINB
 #define B200NORM_NCHW_MINB 4     // resident CTAs per SM the registers allow
 #endif
-constexpr int kNchwThreads = 256;
+#ifndef B200NORM_NCHW_THREADS
+#define B200NORM_NCHW_THREADS 256
+#endif
+constexpr int kNchwThreads = B200NORM_NCHW_THREADS;
 constexpr int kNchwUnroll = B200NORM_NCHW_UNROLL;
 
 template <typename T, typename M, int VE>
