@@ -229,3 +229,19 @@ def units(name) -> int:
     if spec["op"] == "gated_rms":
         return numel // spec["C"]
     return spec["shape"][0] * spec["groups"]
+
+
+def device_normal(shape, dtype, seed, device, mean=0.0, std=1.0):
+    """Seeded N(mean, std) values drawn directly on a CUDA device with torch's
+    generator (float32, then cast to ``dtype``: a torch dtype).  For tensors
+    too large to draw on the host; tests copy the parts they check back to the
+    host for the oracle, so both sides still see the same bits."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    z = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        z.mul_(std)
+    if mean != 0.0:
+        z.add_(mean)
+    return z.to(dtype)
