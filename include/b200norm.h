@@ -38,6 +38,10 @@
  *     the last non-OK status returned on the calling thread.
  *   - Calls are stateless apart from the caller-provided SkipGroupNorm
  *     workspace, and may be issued from several host threads at once.
+ *   - Kernels are launched with programmatic dependent launch allowed: one
+ *     may be scheduled while the previous kernel on the stream drains, but it
+ *     waits for that kernel to complete (and its writes to be visible) before
+ *     touching memory, so stream order is kept.
  */
 #ifndef B200NORM_H
 #define B200NORM_H
