@@ -811,6 +811,8 @@ sgn_normalize(const SgnArgs<T, M> a, int chunks) {
 // ---------------------------------------------------------------------------
 // Kernel selection and typed launch (host)
 // ---------------------------------------------------------------------------
+// Offset (in floats) of the K[groups] | gamma | beta tail of route 2's dynamic
+// shared memory: past both the sums area and the merge area.
 inline size_t coop_k_offset(int PL, int C, int B, int groups) {
   const size_t passes = 2 * (static_cast<size_t>(PL) * C + C);
   const size_t nchunk = (static_cast<size_t>(B) + kCoopMergeChunk - 1) / kCoopMergeChunk;

@@ -120,7 +120,8 @@ static bool allow_smem(void* fn, size_t smem, int dev) {
   return true;
 }
 
-// Offset (in floats) of the K[groups] tail of route 2's shared memory.
+// Dynamic shared memory of route 2: the phase area up to coop_k_offset, then
+// K[groups] (padded to 16 bytes), gamma[C] and beta[C].
 static size_t coop_smem_bytes(int PL, int C, int B, int groups) {
   return (coop_k_offset(PL, C, B, groups) + ((groups + 3) & ~3) + 2ull * C) * sizeof(float);
 }
