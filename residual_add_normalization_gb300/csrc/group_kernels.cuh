@@ -422,7 +422,8 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
 // For NHWC tensors small enough to stay in L2 between two kernels.  Both
 // kernels map blockDim.x = CV * PL threads like route 2 (thread t covers the
 // VE channels (t % CV) * VE .. +VE of pixel lane t / CV) and give CTA b of
-// batch item n = b / B the pixels [(b % B) * kL2Passes * PL, +kL2Passes * PL).
+// batch item n = b / B the pixels [(b % B) * ppc, +ppc), walked kL2Passes
+// pixel lanes at a time; the grid is about what the GPU holds at once.
 //
 // sgn_nhwc_stats forms S (not stored) and accumulates, per group, the sums of
 // S - K[g] and (S - K[g])^2 over its pixels (K[g] the group's first residual
@@ -439,15 +440,13 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
 // Workspace: float4 slots after the control block hold the partials
 // [N * B * groups] and the statistics [N * groups]; the control block holds
 // one counter per batch item (N <= kL2MaxItems), zero between calls.
-constexpr int kL2Passes = 4;       // pixels per thread, statistics kernel
-constexpr int kL2ApplyPasses = 4;  // pixels per thread, apply kernel
+constexpr int kL2Passes = 2;       // pixels per thread in flight
 constexpr int kL2MaxThreads = 512;
 constexpr int64_t kL2RouteMaxBytes = 48ll << 20;  // re-read through the 129 MB L2
-constexpr int64_t kL2MaxPartials = 1ll << 20;     // workspace partial slots
 
 template <typename T, typename M, int VE, bool BC>
 __global__ void __launch_bounds__(kL2MaxThreads, 2)
-sgn_nhwc_stats(const SgnArgs<T, M> a, int B) {
+sgn_nhwc_stats(const SgnArgs<T, M> a, int B, int ppc) {
   pdl_wait();
   pdl_trigger();
   // s_red: per-thread sums [2][VE][PL][CV], later the merge slices [3][S][groups]
@@ -463,27 +462,18 @@ sgn_nhwc_stats(const SgnArgs<T, M> a, int B) {
   const int tp = threadIdx.x / CV;
   const int n = blockIdx.x / B;
   const int b = blockIdx.x % B;
-  const int p0 = b * kL2Passes * PL;
-  const int p1 = min(p0 + kL2Passes * PL, a.HW);
+  const int p0 = b * ppc;
+  const int p1 = min(p0 + ppc, a.HW);
   const int64_t nbase = static_cast<int64_t>(n) * a.HW * C;
   const int c0 = tc * VE;
   const bool active = tp < PL;
 
-  Pack<T, VE> xv[kL2Passes], kv[BC ? 1 : kL2Passes], skb, bv;
+  for (int g = threadIdx.x; g < a.groups; g += blockDim.x) s_K[g] = sgn_shift(a, n, g, true);
+  Pack<T, VE> skb, bv;
   if (active) {
-#pragma unroll
-    for (int k = 0; k < kL2Passes; ++k) {
-      const int p = p0 + tp + k * PL;
-      if (p < p1) {
-        const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
-        xv[k] = ld_reuse<T, VE>(a.x + off);
-        if constexpr (!BC) kv[k] = ld_reuse<T, VE>(a.skip + off);
-      }
-    }
     if constexpr (BC) skb = ld_reuse<T, VE>(a.skip + static_cast<int64_t>(n) * C + c0);
     if (a.bias) bv = ld_reuse<T, VE>(a.bias + c0);
   }
-  for (int g = threadIdx.x; g < a.groups; g += blockDim.x) s_K[g] = sgn_shift(a, n, g, true);
   __syncthreads();
   float s1[VE], s2[VE];
 #pragma unroll
@@ -492,18 +482,29 @@ sgn_nhwc_stats(const SgnArgs<T, M> a, int B) {
     float Kl[VE];
 #pragma unroll
     for (int e = 0; e < VE; ++e) Kl[e] = s_K[(c0 + e) / a.cpg];
+    for (int q = p0 + tp; q < p1; q += kL2Passes * PL) {
+      Pack<T, VE> xv[kL2Passes], kv[BC ? 1 : kL2Passes];
 #pragma unroll
-    for (int k = 0; k < kL2Passes; ++k) {
-      const int p = p0 + tp + k * PL;
-      if (p < p1) {
+      for (int k = 0; k < kL2Passes; ++k) {
+        const int p = q + k * PL;
+        if (p < p1) {
+          const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+          xv[k] = ld_reuse<T, VE>(a.x + off);
+          if constexpr (!BC) kv[k] = ld_reuse<T, VE>(a.skip + off);
+        }
+      }
 #pragma unroll
-        for (int e = 0; e < VE; ++e) {
-          const float sk = BC ? to_f32(skb.v[e]) : to_f32(kv[BC ? 0 : k].v[e]);
-          const float d =
-              to_f32(sgn_sum_b<T>(to_f32(xv[k].v[e]), sk, to_f32(bv.v[e]), a.bias != nullptr)) -
-              Kl[e];
-          s1[e] += d;
-          s2[e] = fmaf(d, d, s2[e]);
+      for (int k = 0; k < kL2Passes; ++k) {
+        if (q + k * PL < p1) {
+#pragma unroll
+          for (int e = 0; e < VE; ++e) {
+            const float sk = BC ? to_f32(skb.v[e]) : to_f32(kv[BC ? 0 : k].v[e]);
+            const float d = to_f32(sgn_sum_b<T>(to_f32(xv[k].v[e]), sk, to_f32(bv.v[e]),
+                                                a.bias != nullptr)) -
+                            Kl[e];
+            s1[e] += d;
+            s2[e] = fmaf(d, d, s2[e]);
+          }
         }
       }
     }
@@ -601,28 +602,29 @@ sgn_nhwc_stats(const SgnArgs<T, M> a, int B) {
 
 template <typename T, typename M, int VE, bool BC>
 __global__ void __launch_bounds__(kL2MaxThreads, 2)
-sgn_nhwc_apply(const SgnArgs<T, M> a, int B, int B2) {
-  extern __shared__ float4 s_st[];  // [groups] (K, d, rstd, -) | gamma[C] | beta[C]
-  float* s_ga = reinterpret_cast<float*>(s_st + a.groups);
-  float* s_be = s_ga + a.C;
+sgn_nhwc_apply(const SgnArgs<T, M> a, int B, int ppc) {
+  // per channel c, at [(c % VE) * CV + c / VE] (the threads of a warp read
+  // consecutive entries): (K, d, rstd * gamma[c], beta[c]) of c's group
+  extern __shared__ float4 s_coef[];
   const int C = a.C;
   const int CV = C / VE;
   const int PL = blockDim.x / CV;
   const int tc = threadIdx.x % CV;
   const int tp = threadIdx.x / CV;
-  const int n = blockIdx.x / B2;
-  const int b = blockIdx.x % B2;
-  const int p0 = b * kL2ApplyPasses * PL;
-  const int p1 = min(p0 + kL2ApplyPasses * PL, a.HW);
+  const int n = blockIdx.x / B;
+  const int b = blockIdx.x % B;
+  const int p0 = b * ppc;
+  const int p1 = min(p0 + ppc, a.HW);
   const int64_t nbase = static_cast<int64_t>(n) * a.HW * C;
   const int c0 = tc * VE;
   const bool active = tp < PL;
-  // Inputs first: the kernel before this one (the statistics kernel) writes
-  // none of them, and it waited for everything before it.
-  Pack<T, VE> xv[kL2ApplyPasses], kv[BC ? 1 : kL2ApplyPasses], skb, bv;
+  // The first pixels' inputs before the wait: the kernel before this one (the
+  // statistics kernel) writes none of them, and it waited for everything
+  // before it.
+  Pack<T, VE> xv[kL2Passes], kv[BC ? 1 : kL2Passes], skb, bv;
   if (active) {
 #pragma unroll
-    for (int k = 0; k < kL2ApplyPasses; ++k) {
+    for (int k = 0; k < kL2Passes; ++k) {
       const int p = p0 + tp + k * PL;
       if (p < p1) {
         const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
@@ -633,37 +635,44 @@ sgn_nhwc_apply(const SgnArgs<T, M> a, int B, int B2) {
     if constexpr (BC) skb = ld_reuse<T, VE>(a.skip + static_cast<int64_t>(n) * C + c0);
     if (a.bias) bv = ld_reuse<T, VE>(a.bias + c0);
   }
-  for (int c = threadIdx.x; c < C; c += blockDim.x) {
-    s_ga[c] = to_f32(__ldg(a.gamma + c));
-    s_be[c] = to_f32(__ldg(a.beta + c));
-  }
   pdl_wait();
   pdl_trigger();
   const float4* stats = a.part + a.N * B * a.groups + static_cast<int64_t>(n) * a.groups;
-  for (int g = threadIdx.x; g < a.groups; g += blockDim.x) s_st[g] = __ldcg(stats + g);
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    const float4 st = __ldcg(stats + c / a.cpg);
+    s_coef[(c % VE) * CV + c / VE] =
+        make_float4(st.x, st.y, st.z * to_f32(__ldg(a.gamma + c)), to_f32(__ldg(a.beta + c)));
+  }
   __syncthreads();
   if (!active) return;
-  int gi[VE];
+  for (int q = p0 + tp; q < p1; q += kL2Passes * PL) {
+    if (q != p0 + tp) {
 #pragma unroll
-  for (int e = 0; e < VE; ++e) gi[e] = (c0 + e) / a.cpg;
-#pragma unroll
-  for (int k = 0; k < kL2ApplyPasses; ++k) {
-    const int p = p0 + tp + k * PL;
-    if (p < p1) {
-      const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
-      Pack<T, VE> sv, out;
-      float ga[VE], be[VE];
-      lds_vec<VE>(s_ga + c0, ga);
-      lds_vec<VE>(s_be + c0, be);
-#pragma unroll
-      for (int e = 0; e < VE; ++e) {
-        const float sk = BC ? to_f32(skb.v[e]) : to_f32(kv[BC ? 0 : k].v[e]);
-        sv.v[e] = sgn_sum_b<T>(to_f32(xv[k].v[e]), sk, to_f32(bv.v[e]), a.bias != nullptr);
-        const float4 st = s_st[gi[e]];
-        out.v[e] = from_f32<T>(sgn_out(to_f32(sv.v[e]), st.x, st.y, st.z, ga[e], be[e], a.act));
+      for (int k = 0; k < kL2Passes; ++k) {
+        const int p = q + k * PL;
+        if (p < p1) {
+          const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+          xv[k] = ld_stream<T, VE>(a.x + off);
+          if constexpr (!BC) kv[k] = ld_stream<T, VE>(a.skip + off);
+        }
       }
-      if (a.s) st_stream<T, VE>(a.s + off, sv);
-      st_stream<T, VE>(a.y + off, out);
+    }
+#pragma unroll
+    for (int k = 0; k < kL2Passes; ++k) {
+      const int p = q + k * PL;
+      if (p < p1) {
+        const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+        Pack<T, VE> sv, out;
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          const float sk = BC ? to_f32(skb.v[e]) : to_f32(kv[BC ? 0 : k].v[e]);
+          sv.v[e] = sgn_sum_b<T>(to_f32(xv[k].v[e]), sk, to_f32(bv.v[e]), a.bias != nullptr);
+          const float4 cf = s_coef[e * CV + tc];
+          out.v[e] = from_f32<T>(sgn_out(to_f32(sv.v[e]), cf.x, cf.y, cf.z, 1.0f, cf.w, a.act));
+        }
+        if (a.s) st_stream<T, VE>(a.s + off, sv);
+        st_stream<T, VE>(a.y + off, out);
+      }
     }
   }
 }
@@ -939,19 +948,15 @@ inline cudaError_t launch_group_typed(const SkipGroupCall& c, const GroupPlan& p
   if (p.route == 4) {
     void *stats = nullptr, *apply = nullptr;
     pick_l2<T, M>(p.ve, c.bcast, &stats, &apply);
-    int B = p.ctas_per_item;
-    const int PL = p.block / static_cast<int>(c.C / p.ve);
-    int B2 = static_cast<int>((c.H * c.W + kL2ApplyPasses * PL - 1) / (kL2ApplyPasses * PL));
-    void* args1[] = {&a, &B};
-    void* args2[] = {&a, &B, &B2};
+    int B = p.ctas_per_item, ppc = p.pix_per_cta;
+    void* args[] = {&a, &B, &ppc};
     cfg.attrs = attr;
     cfg.numAttrs = add_pdl_attr(attr, 0);
     cfg.dynamicSmemBytes = static_cast<size_t>(c.groups) * sizeof(float);
-    cudaError_t e = cudaLaunchKernelExC(&cfg, stats, args1);
+    cudaError_t e = cudaLaunchKernelExC(&cfg, stats, args);
     if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(static_cast<unsigned>(c.N * B2));
     cfg.dynamicSmemBytes = p.smem;
-    return cudaLaunchKernelExC(&cfg, apply, args2);
+    return cudaLaunchKernelExC(&cfg, apply, args);
   }
   // route 3
   int chunks = p.chunks;

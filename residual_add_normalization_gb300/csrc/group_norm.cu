@@ -2,6 +2,8 @@
 // grid-barrier timeout probe.  The kernels are in group_kernels.cuh,
 // instantiated per element type in group_f32.cu / group_f16.cu /
 // group_bf16.cu.
+#include <algorithm>
+
 #include "group_kernels.cuh"
 
 namespace b200norm {
@@ -19,22 +21,12 @@ __global__ void barrier_timeout_probe(Control* ctl, unsigned long long limit_ns)
 // ---------------------------------------------------------------------------
 static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Route 4 geometry for vectors of `ve` elements: false when the route does
-// not apply (channels per CTA row, shared-memory tables or partial count out
-// of range).  `in_bytes` is what the second kernel re-reads through L2.
-static bool l2_route_shape(int64_t N, int64_t C, int64_t HW, int groups, int ve,
-                           int64_t in_bytes, int* PL, int64_t* B) {
-  if (N > kL2MaxItems || C % ve != 0 || C > 1024 || in_bytes > kL2RouteMaxBytes) return false;
-  const int64_t CV = C / ve;
-  if (CV > kL2MaxThreads) return false;
-  *PL = static_cast<int>(kL2MaxThreads / CV);
-  *B = cdiv(HW, static_cast<int64_t>(kL2Passes) * *PL);
-  return N * *B * groups <= kL2MaxPartials;
-}
-
-// Workspace slots of route 4 (partials and statistics).
-static int64_t l2_route_slots(int64_t N, int64_t B, int groups) {
-  return N * B * groups + N * groups;
+// Does route 4 take vectors of `ve` elements here?  (batch items the control
+// block counts, channels per CTA row, shared-memory tables, and what the
+// second kernel re-reads through L2: `in_bytes`.)
+static bool l2_route_ok(int64_t N, int64_t C, int ve, int64_t in_bytes) {
+  return N <= kL2MaxItems && C % ve == 0 && C <= 1024 && C / ve <= kL2MaxThreads &&
+         in_bytes <= kL2RouteMaxBytes;
 }
 
 size_t group_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int groups, DType t) {
@@ -45,10 +37,9 @@ size_t group_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int gro
   int64_t slots = two_phase > coop ? two_phase : coop;
   const int64_t es = static_cast<int64_t>(dtype_size(t));
   for (int ve : {1, static_cast<int>(16 / es)}) {
-    int PL = 0;
-    int64_t B = 0;
-    if (l2_route_shape(N, C, H * W, groups, ve, N * H * W * C * es, &PL, &B)) {
-      const int64_t r4 = l2_route_slots(N, B, groups);
+    // route 4: at most kMaxCoopCtas partials per group, then the statistics
+    if (l2_route_ok(N, C, ve, N * H * W * C * es)) {
+      const int64_t r4 = static_cast<int64_t>(kMaxCoopCtas) * groups + N * groups;
       if (r4 > slots) slots = r4;
     }
   }
@@ -148,11 +139,20 @@ static bool plan_l2_route(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) 
   const int vec = static_cast<int>(16 / es);
   const int ve = (vector_ok && c.C % vec == 0) ? vec : 1;
   const int64_t numel = c.N * c.H * c.W * c.C;
-  int PL = 0;
-  int64_t B = 0;
-  if (!l2_route_shape(c.N, c.C, c.H * c.W, c.groups, ve, numel * es * (c.bcast ? 1 : 2), &PL,
-                      &B))
+  if (!l2_route_ok(c.N, c.C, ve, numel * es * (c.bcast ? 1 : 2))) return false;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
     return false;
+  }
+  // about two CTAs per SM over the whole grid, each walking its pixel range
+  const int64_t HW = c.H * c.W;
+  const int PL = static_cast<int>(kL2MaxThreads / (c.C / ve));
+  const int64_t target = std::min<int64_t>(2LL * sms, kMaxCoopCtas);
+  int64_t B = std::min<int64_t>(cdiv(HW, PL), std::max<int64_t>(1, target / c.N));
+  const int64_t ppc = cdiv(HW, B);
+  B = cdiv(HW, ppc);
   *p = GroupPlan{};
   p->route = 4;
   p->ve = ve;
@@ -161,8 +161,8 @@ static bool plan_l2_route(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) 
   p->csize = 1;
   p->grid = c.N * B;
   p->ctas_per_item = static_cast<int>(B);
-  p->pix_per_cta = kL2Passes * PL;
-  p->smem = static_cast<size_t>(c.groups) * sizeof(float4) + 2 * c.C * sizeof(float);
+  p->pix_per_cta = static_cast<int>(ppc);
+  p->smem = static_cast<size_t>(c.C) * sizeof(float4);
   return true;
 }
 
