@@ -340,8 +340,8 @@ __device__ __forceinline__ void pdl_trigger() {
 // zero), so one workspace serves calls of any shape in turn.
 constexpr int kL2MaxItems = 56;  // batch items of the NHWC L2 route
 struct Control {
-  unsigned int bar_count;  // CTAs arrived at the current barrier (0 between barriers)
-  unsigned int bar_gen;    // barrier generation
+  unsigned int bar_count;  // CTAs arrived at the grid barrier (0 between launches)
+  unsigned int bar_gen;    // CTAs that have left the grid barrier (0 between launches)
   unsigned int error;      // 0, or a b200norm_status recorded by a kernel
   unsigned int error_site; // which wait gave up
   unsigned int item_done[kL2MaxItems];  // NHWC L2 route: CTAs of item n done
@@ -356,15 +356,8 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
-               : "memory");
-  return old;
-}
-
-__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
@@ -373,37 +366,53 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
-// All `expected` CTAs of the grid call this once per barrier.  The last CTA to
-// arrive resets the count and bumps the generation, so the control block is
-// left ready for the next barrier or call.  A CTA that waits longer than
-// `limit_ns` records a timeout and returns false; the caller must then stop.
-__device__ __forceinline__ bool grid_barrier(Control* ctl, unsigned expected,
-                                             unsigned long long limit_ns, unsigned site) {
-  __shared__ int ok;
+// A grid barrier used once per launch, in three parts, so that a CTA can do
+// work that no other CTA needs (stores of results only it reads) between its
+// arrival and its wait.  Control::bar_count counts arrivals and
+// Control::bar_gen departures; both are 0 before the launch, and the CTA that
+// departs last puts them back to 0 at its end (every CTA has then left its
+// wait), so the next launch finds them ready.
+//
+// grid_arrive publishes every thread's earlier writes to the CTAs that return
+// from grid_wait (a release add; the waiters' acquire load reads the count the
+// chain of adds produced).  grid_wait waits for `expected` arrivals; after
+// `limit_ns` it records a timeout and returns false, and the caller must stop
+// after calling grid_depart.  Every CTA of the grid takes a departure ticket
+// in grid_wait, whether it timed out or not, and passes it (meaningful in
+// thread 0) to grid_depart once it has finished, so that it does not wait for
+// that atomic in between; the counts are reset even after a timeout, and the
+// error stays recorded until the workspace is initialised again.
+__device__ __forceinline__ void grid_arrive(Control* ctl) {
   __syncthreads();  // every thread's earlier writes are ordered before thread 0's release
+  if (threadIdx.x == 0) red_add_release_gpu(&ctl->bar_count, 1u);
+}
+
+__device__ __forceinline__ bool grid_wait(Control* ctl, unsigned expected,
+                                          unsigned long long limit_ns, unsigned site,
+                                          unsigned& departure) {
+  __shared__ int ok;
   if (threadIdx.x == 0) {
-    const unsigned gen = ld_acquire_gpu(&ctl->bar_gen);
-    // arrive: release publishes this CTA's writes, acquire (for the last
-    // arrival) sees every other CTA's
-    const unsigned arrived = atom_add_acq_rel_gpu(&ctl->bar_count, 1u) + 1u;
     ok = 1;
-    if (arrived == expected) {
-      ctl->bar_count = 0u;                      // ordered before the release below
-      st_release_gpu(&ctl->bar_gen, gen + 1u);  // opens the barrier
-    } else {
-      const unsigned long long t0 = global_ns();
-      while (ld_acquire_gpu(&ctl->bar_gen) == gen) {
-        if (global_ns() - t0 > limit_ns) {
-          atomicExch(&ctl->error, kStatusDeviceTimeout);
-          atomicExch(&ctl->error_site, site);
-          ok = 0;
-          break;
-        }
+    const unsigned long long t0 = global_ns();
+    while (ld_acquire_gpu(&ctl->bar_count) < expected) {
+      if (global_ns() - t0 > limit_ns) {
+        atomicExch(&ctl->error, kStatusDeviceTimeout);
+        atomicExch(&ctl->error_site, site);
+        ok = 0;
+        break;
       }
     }
+    departure = atomicAdd(&ctl->bar_gen, 1u);
   }
   __syncthreads();
   return ok != 0;
+}
+
+__device__ __forceinline__ void grid_depart(Control* ctl, unsigned departure) {
+  if (threadIdx.x == 0 && departure == gridDim.x - 1u) {
+    ctl->bar_count = 0u;
+    ctl->bar_gen = 0u;
+  }
 }
 
 }  // namespace b200norm

@@ -242,9 +242,10 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
 // Every CTA takes, per group, the count and the sums of S - K[g] and
 // (S - K[g])^2 over the S it holds (K[g] the group's first residual sum, the
 // same in every CTA, so the shifted sums do not cancel): per thread, per
-// pixel lane and channel, then per group.  After one grid barrier each CTA adds
-// its batch item's partials in a fixed order: mean = K + d,
-// var = sum((S - K)^2) / n - d^2.
+// pixel lane and channel, then per group.  It stores S between its arrival at
+// the grid barrier and its wait.  After the barrier each CTA adds its batch
+// item's partials in a fixed order, mean = K + d,
+// var = sum((S - K)^2) / n - d^2, and stores Y.
 // Dynamic shared memory (floats), layout given by k_offset:
 //   sums:    acc[2][PL*C] | col[2][C]
 //   merge:   chunk sums[nchunk*groups*3] | mean offset d[groups] | rstd[groups]
@@ -270,7 +271,7 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
   const int64_t nbase = static_cast<int64_t>(n) * a.HW * C;
   const int c0 = tc * VE;
 
-  // --- load and form S (S is stored after the barrier, with Y) ------------
+  // --- load and form S (stored while the grid barrier is pending) ----------
   Pack<T, VE> xv[NV], kv[NV], sv[NV];
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
@@ -345,8 +346,21 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
     }
     a.part[static_cast<int64_t>(blockIdx.x) * a.groups + gg] = make_float4(n_cta, t1, t2, 0.0f);
   }
-  // the barrier's release (after a CTA barrier) publishes these partials
-  if (!grid_barrier(a.ctl, gridDim.x, a.limit_ns, 1u)) return;
+  // the arrival's release (after a CTA barrier) publishes these partials; S,
+  // which no other CTA reads, is stored while the other CTAs arrive
+  grid_arrive(a.ctl);
+  if (a.s) {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int p = p0 + tp + k * PL;
+      if (p < p1) st_stream<T, VE>(a.s + nbase + static_cast<int64_t>(p) * C + c0, sv[k]);
+    }
+  }
+  unsigned departure = 0u;
+  if (!grid_wait(a.ctl, gridDim.x, a.limit_ns, 1u, departure)) {
+    grid_depart(a.ctl, departure);
+    return;
+  }
 
   // --- add the batch item's B partials per group (every CTA shifts by the
   // same K, so plain sums in a fixed order) -----------------------------------
@@ -390,7 +404,7 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
     s_grstd[gg] = 1.0f / sqrtf(fmaxf(c2 / cn - d * d, 0.0f) + a.eps);
   }
   __syncthreads();
-  // --- normalize what this thread holds; store S and Y ---------------------
+  // --- normalize what this thread holds; store Y ---------------------------
   float mu[VE], rs[VE];
 #pragma unroll
   for (int e = 0; e < VE; ++e) {
@@ -402,7 +416,6 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
     const int p = p0 + tp + k * PL;
     if (p < p1) {
       const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
-      if (a.s) st_stream<T, VE>(a.s + off, sv[k]);
       float ga[VE], be[VE];
       lds_vec<VE>(s_ga + c0, ga);
       lds_vec<VE>(s_be + c0, be);
@@ -414,6 +427,7 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
       st_stream<T, VE>(a.y + off, out);
     }
   }
+  grid_depart(a.ctl, departure);
 }
 
 // ---------------------------------------------------------------------------

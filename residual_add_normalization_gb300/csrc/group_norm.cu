@@ -13,7 +13,10 @@ namespace b200norm {
 // the grid has).  Every CTA gives up after limit_ns and records a timeout.
 // ---------------------------------------------------------------------------
 __global__ void barrier_timeout_probe(Control* ctl, unsigned long long limit_ns) {
-  grid_barrier(ctl, gridDim.x + 1, limit_ns, 99u);
+  unsigned departure = 0u;
+  grid_arrive(ctl);
+  grid_wait(ctl, gridDim.x + 1, limit_ns, 99u, departure);
+  grid_depart(ctl, departure);
 }
 
 // ---------------------------------------------------------------------------

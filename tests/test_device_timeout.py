@@ -33,6 +33,9 @@ def test_unsatisfiable_barrier_reports_timeout_and_context_survives():
     assert elapsed < 10.0
     with pytest.raises(b2.B200NormError):
         b2.workspace_status(ws)
+    # every CTA left the barrier after giving up, so the counts are back at zero
+    ctl = ws[:16].view(torch.int32).cpu().numpy()
+    assert ctl[0] == 0 and ctl[1] == 0 and ctl[2] == TIMEOUT
     # re-initialise, then the same workspace serves a real call
     b2.workspace_init(ws)
     b2.workspace_status(ws)
@@ -49,16 +52,34 @@ def test_unsatisfiable_barrier_reports_timeout_and_context_survives():
 
 def test_workspace_left_ready_after_many_calls():
     """The cooperative route's barrier resets itself: many back-to-back calls
-    on one workspace keep working and leave no error."""
-    ws = torch.zeros(b2.workspace_size(2, 320, 64, 64, 32), dtype=torch.uint8, device="cuda")
-    d = synthetic.skip_group_inputs((2, 64, 64, 320), np.float16, np.float32, seed=3,
-                                    channels_last=1, skip="nc", bias=True)
-    args = [to_dev(d[k]) for k in ("x", "skip", "gamma", "beta", "bias")]
-    for _ in range(50):
-        y, _ = b2.skip_group(*args, groups=32, activation=1, workspace=ws)
+    on one workspace, alternating two shapes whose cooperative grids differ in
+    size, keep working and leave the arrival and departure counts at zero and
+    no error."""
+    shapes = [((2, 64, 64, 320), 32), ((1, 16, 16, 512), 16)]
+    grids = set()
+    for (N, H, W, C), G in shapes:
+        out = (ctypes.c_int64 * 8)()
+        # float16 X, float32 gamma/beta, NHWC, 16-byte aligned
+        assert b2.library().b200norm_testing_plan_group(N, C, H, W, G, 1, 0, 1, 1, out) == 0
+        assert out[0] == 2  # the cooperative route
+        grids.add(out[5])
+    assert len(grids) == 2
+    ws = torch.zeros(max(b2.workspace_size(N, C, H, W, G, torch.float16, 1)
+                         for (N, H, W, C), G in shapes), dtype=torch.uint8, device="cuda")
+    cases = []
+    for k, (shape, G) in enumerate(shapes):
+        d = synthetic.skip_group_inputs(shape, np.float16, np.float32, seed=3 + k,
+                                        channels_last=1, skip="nc", bias=True)
+        cases.append((d, G, [to_dev(d[key]) for key in ("x", "skip", "gamma", "beta", "bias")]))
+    ys = [None, None]
+    for i in range(50):
+        d, G, args = cases[i % 2]
+        ys[i % 2], _ = b2.skip_group(*args, groups=G, activation=1, channels_last=1, workspace=ws)
     b2.workspace_status(ws)
     ctl = ws[:16].view(torch.int32).cpu().numpy()
-    assert ctl[0] == 0 and ctl[2] == 0  # count back at zero, no error recorded
-    ry, _ = oracle.skip_group(d["x"], d["skip"], d["gamma"], d["beta"], d["bias"], groups=32,
-                              activation=1)
-    assert_y_close(to_host(y), ry)
+    # arrivals and departures back at zero, no error recorded
+    assert ctl[0] == 0 and ctl[1] == 0 and ctl[2] == 0
+    for (d, G, _), y in zip(cases, ys):
+        ry, _ = oracle.skip_group(d["x"], d["skip"], d["gamma"], d["beta"], d["bias"], groups=G,
+                                  activation=1, channels_last=1)
+        assert_y_close(to_host(y), ry)
