@@ -152,6 +152,18 @@ B200NORM_API b200norm_status b200norm_gated_rms(const void* x, const void* gate,
                                                 int64_t C, b200norm_dtype T, float epsilon,
                                                 b200norm_stream_t stream);
 
+/* Synchronise `stream`, then read the device-side record of the pipelined row
+ * schedule on the current device.  SkipSimplifiedLayerNormalization and
+ * GatedRMSNorm calls with short rows (at most 32 16-byte vectors) may run a
+ * kernel that streams its inputs through shared memory; its waits on copy
+ * completion are bounded (about one second), and one that gives up records
+ * B200NORM_ERR_DEVICE_TIMEOUT in a per-device word and returns early (that
+ * call's outputs are then undefined).  Returns B200NORM_OK, or
+ * B200NORM_ERR_DEVICE_TIMEOUT (and clears the record) if any such launch on
+ * the device gave up since the last call; B200NORM_ERR_CUDA if the read
+ * failed.  No correct launch records anything. */
+B200NORM_API b200norm_status b200norm_rows_status(b200norm_stream_t stream);
+
 /*
  * SkipGroupNorm (com.microsoft.SkipGroupNorm README: Description, Inputs,
  * Outputs, Attributes, Type constraints):

@@ -23,7 +23,13 @@ B200NORM_API b200norm_status b200norm_testing_barrier_timeout(void* workspace,
                                                               b200norm_stream_t stream);
 
 /* Force a schedule on the calling thread (0 = automatic choice):
- *   row_mode:    2 = walk each row twice (any row length)
+ *   row_mode:    1 = register-resident schedules only (never the pipelined
+ *                    one that automatic choice gives long runs of short
+ *                    SkipSimplifiedLayerNormalization rows)
+ *                2 = walk each row twice (any row length)
+ *                3 = pipelined lane groups (rows of at most 32 16-byte
+ *                    vectors with 16-byte aligned tensors; other calls return
+ *                    B200NORM_ERR_UNSUPPORTED)
  *   group_route: 2 = NHWC cooperative grid with one bounded grid barrier
  *                3 = two-phase partials -> normalize (any shape)
  *                4 = NHWC through L2 (statistics kernel, then apply kernel)
@@ -46,6 +52,13 @@ B200NORM_API b200norm_status b200norm_testing_force_split(int csize, int nv);
  * may be scheduled while the preceding grid on its stream drains and waits
  * for that grid before touching memory; results are identical either way. */
 B200NORM_API b200norm_status b200norm_testing_set_pdl(int on);
+
+/* Stall the pipelined row schedule (process-wide) for later launches: with
+ * on = 1 its producer issues no copies, so every consumer wait gives up after
+ * limit_ns (in (0, 5 s]) and the kernel records B200NORM_ERR_DEVICE_TIMEOUT
+ * (read with b200norm_rows_status) with nothing in flight; outputs are left
+ * unwritten.  on = 0 restores normal launches (limit_ns ignored). */
+B200NORM_API b200norm_status b200norm_testing_pipe_stall(int on, uint64_t limit_ns);
 
 /* Schedule the automatic planner picks, without launching anything.
  * Rows (SSLN / GatedRMSNorm): out = {mode, ve, tpr, nv, rpg, block, csize, grid}.

@@ -77,10 +77,12 @@ def library() -> ctypes.CDLL:
                                      vp, sz, vp], i32),
             "b200norm_workspace_init": ([vp, sz, vp], i32),
             "b200norm_workspace_status": ([vp, vp], i32),
+            "b200norm_rows_status": ([vp], i32),
             "b200norm_testing_barrier_timeout": ([vp, sz, ctypes.c_uint64, vp], i32),
             "b200norm_testing_force": ([i32, i32], i32),
             "b200norm_testing_force_split": ([i32, i32], i32),
             "b200norm_testing_set_pdl": ([i32], i32),
+            "b200norm_testing_pipe_stall": ([i32, ctypes.c_uint64], i32),
             "b200norm_testing_plan_rows": ([i64, i64, i32, i32, ctypes.POINTER(ctypes.c_int64)],
                                            i32),
             "b200norm_testing_plan_group": ([i64, i64, i64, i64, i32, i32, i32, i32, i32,
@@ -216,6 +218,16 @@ def gated_rms(x, gate, scale, *, epsilon=1e-5, y=None, stream=None):
 
 _workspaces = {}
 _ws_lock = threading.Lock()
+
+
+def rows_status(stream=None, device=None):
+    """Synchronizes ``stream`` and raises B200NormError if a pipelined row
+    kernel (short SkipSimplifiedLayerNormalization / GatedRMSNorm rows) on the
+    device gave up a bounded wait since the last call; the record is then
+    cleared."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        _check(library().b200norm_rows_status(_stream(dev, stream)))
 
 
 def workspace_size(N, C, H, W, groups, dtype=torch.float16, channels_last=1) -> int:

@@ -156,7 +156,11 @@ b200norm_status skip_rms_impl(const void* input, const void* skip, const void* g
   RowPlan plan = plan_rows(rows, hidden, to_dtype(T), vec);
   if (g_force_csize)
     if (b200norm_status st = forced_split(rows, hidden, &plan)) return st;
+  if (g_force_row_mode == 0 && !g_force_csize)
+    prefer_pipe_skip_rms(rows, hidden, to_dtype(T), vec, &plan);
   if (g_force_row_mode == 2) plan = forced_walk(rows, plan);
+  if (g_force_row_mode == 3 && !pipe_plan(rows, hidden, to_dtype(T), vec, &plan))
+    return fail(B200NORM_ERR_UNSUPPORTED, "forced pipelined schedule cannot take this call");
   if (plan.grid > kMaxGrid) return fail(B200NORM_ERR_UNSUPPORTED, "too many rows for one launch");
   SkipRmsCall c{input, skip, gamma, bias, output, sum, mean, inv_std, rows, hidden, to_dtype(T),
                 epsilon};
@@ -264,6 +268,8 @@ b200norm_status b200norm_gated_rms(const void* x, const void* gate, const void* 
   if (g_force_csize)
     if (b200norm_status st = forced_split(rows, C, &plan)) return st;
   if (g_force_row_mode == 2) plan = forced_walk(rows, plan);
+  if (g_force_row_mode == 3 && !pipe_plan(rows, C, to_dtype(T), vec, &plan))
+    return fail(B200NORM_ERR_UNSUPPORTED, "forced pipelined schedule cannot take this call");
   if (plan.grid > kMaxGrid) return fail(B200NORM_ERR_UNSUPPORTED, "too many rows for one launch");
   GatedCall c{x, gate, scale, y, rows, C, to_dtype(T), epsilon};
   cudaError_t e = launch_gated(c, plan, reinterpret_cast<cudaStream_t>(stream));
@@ -371,6 +377,21 @@ b200norm_status b200norm_workspace_status(const void* workspace, b200norm_stream
   return ok();
 }
 
+b200norm_status b200norm_rows_status(b200norm_stream_t stream) {
+  unsigned* word = pipe_status_word();
+  if (!word) return fail(B200NORM_ERR_CUDA, "row status word not available on this device");
+  unsigned v = 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&v, word, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && v != 0) e = cudaMemsetAsync(word, 0, sizeof(v), st);
+  if (e == cudaSuccess && v != 0) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "row status read");
+  if (v != 0) return fail(static_cast<b200norm_status>(v), "a pipelined row wait gave up");
+  return ok();
+}
+
 // ---- testing hooks ---------------------------------------------------------
 
 b200norm_status b200norm_testing_barrier_timeout(void* workspace, size_t workspace_bytes,
@@ -386,9 +407,10 @@ b200norm_status b200norm_testing_barrier_timeout(void* workspace, size_t workspa
 }
 
 b200norm_status b200norm_testing_force(int row_mode, int group_route) {
-  if ((row_mode != 0 && row_mode != 2) ||
+  if (row_mode < 0 || row_mode > 3 ||
       (group_route != 0 && group_route != 2 && group_route != 3 && group_route != 4))
-    return fail(B200NORM_ERR_INVALID_ARGUMENT, "row_mode in {0, 2}, group_route in {0, 2, 3, 4}");
+    return fail(B200NORM_ERR_INVALID_ARGUMENT,
+                "row_mode in {0, 1, 2, 3}, group_route in {0, 2, 3, 4}");
   g_force_row_mode = row_mode;
   g_force_group_route = group_route;
   return ok();
@@ -403,6 +425,13 @@ b200norm_status b200norm_testing_force_split(int csize, int nv) {
                 "csize in {1, 2, 4, 8, 16} and nv in {1, 2, 4, 8}, or both 0");
   g_force_csize = csize;
   g_force_nv = nv;
+  return ok();
+}
+
+b200norm_status b200norm_testing_pipe_stall(int on, uint64_t limit_ns) {
+  if ((on != 0 && on != 1) || (on && (limit_ns == 0 || limit_ns > 5000000000ull)))
+    return fail(B200NORM_ERR_INVALID_ARGUMENT, "on in {0, 1}; with on, limit_ns in (0, 5 s]");
+  set_pipe_stall(on != 0, on ? limit_ns : 0);
   return ok();
 }
 

@@ -18,7 +18,8 @@
 //                            the row twice (the second pass is served by L2).
 //
 // Op policies (SkipRmsOp, GatedOp) supply the per-vector load / combine /
-// finish steps; the schedule code is shared.
+// finish steps; the schedule code is shared.  rows_pipe.cuh adds a fourth
+// schedule for short spans that streams both inputs through shared memory.
 #pragma once
 
 #include "common.cuh"
@@ -71,6 +72,7 @@ __device__ __forceinline__ float row_rstd(float sumsq, float inv_n, float eps) {
 template <typename T, int VE, bool HAS_BIAS, bool WANT_S>
 struct SkipRmsOp {
   using Args = SkipRmsArgs<T>;
+  using Elem = T;
   using P = Pack<T, VE>;
   static constexpr int kVE = VE;
   struct In {
@@ -80,6 +82,14 @@ struct SkipRmsOp {
     P gamma, bias;
   };
   using Hold = P;
+
+  // the two streamed inputs, for the pipelined schedule
+  __device__ static __forceinline__ const T* src0(const Args& a) { return a.x; }
+  __device__ static __forceinline__ const T* src1(const Args& a) { return a.skip; }
+  __device__ static __forceinline__ void load_pair(const P& p0, const P& p1, In& in) {
+    in.x = p0;
+    in.k = p1;
+  }
 
   __device__ static __forceinline__ void load_wt(const Args& a, int v, Wt& w) {
     w.gamma = ld_reuse<T, VE>(a.gamma + v * VE);
@@ -157,6 +167,7 @@ struct SkipRmsOp {
 template <typename T, int VE>
 struct GatedOp {
   using Args = GatedArgs<T>;
+  using Elem = T;
   using P = Pack<T, VE>;
   static constexpr int kVE = VE;
   struct In {
@@ -166,6 +177,14 @@ struct GatedOp {
     P scale;
   };
   using Hold = In;
+
+  // the two streamed inputs, for the pipelined schedule
+  __device__ static __forceinline__ const T* src0(const Args& a) { return a.x; }
+  __device__ static __forceinline__ const T* src1(const Args& a) { return a.gate; }
+  __device__ static __forceinline__ void load_pair(const P& p0, const P& p1, In& in) {
+    in.x = p0;
+    in.g = p1;
+  }
 
   __device__ static __forceinline__ void load_wt(const Args& a, int v, Wt& w) {
     w.scale = ld_reuse<T, VE>(a.scale + v * VE);

@@ -86,6 +86,62 @@ RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok) {
   return p;
 }
 
+bool pipe_plan(int64_t rows, int64_t n, DType t, bool vector_ok, RowPlan* p) {
+  const int ve = static_cast<int>(16 / dtype_size(t));
+  if (!vector_ok || n % ve != 0 || n / ve > 32 || rows <= 0) return false;
+  *p = RowPlan{};
+  p->mode = 3;
+  p->ve = ve;
+  p->tpr = pow2_ceil(n / ve);
+  p->nv = 1;
+  p->rpg = 1;
+  p->block = kPipeThreads;
+  p->csize = 1;
+  p->grid = ceil_div(rows, static_cast<int64_t>(kPipeWarps) * (32 / p->tpr));  // tiles
+  return true;
+}
+
+bool prefer_pipe_skip_rms(int64_t rows, int64_t n, DType t, bool vector_ok, RowPlan* p) {
+  RowPlan q;
+  if (!pipe_plan(rows, n, t, vector_ok, &q) ||
+      q.grid < (t == DType::F16 ? kPipeMinTilesF16 : kPipeMinTiles))
+    return false;
+  *p = q;
+  return true;
+}
+
+// The pipelined schedule's status word (one per device) and testing stall.
+__device__ unsigned g_pipe_status;
+static std::atomic<bool> g_pipe_stall{false};
+static std::atomic<unsigned long long> g_pipe_stall_limit_ns{kPipeLimitNs};
+
+unsigned* pipe_status_word() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<unsigned*> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  unsigned* p = cache[dev].load();
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_pipe_status) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  p = static_cast<unsigned*>(addr);
+  cache[dev].store(p);
+  return p;
+}
+
+bool pipe_stalled() { return g_pipe_stall.load(); }
+unsigned long long pipe_stall_limit_ns() { return g_pipe_stall_limit_ns.load(); }
+void set_pipe_stall(bool on, unsigned long long limit_ns) {
+  g_pipe_stall_limit_ns.store(limit_ns);
+  g_pipe_stall.store(on);
+}
+
 cudaError_t launch_skip_rms(const SkipRmsCall& c, const RowPlan& p, cudaStream_t st) {
   switch (c.t) {
     case DType::F32: return skip_rms_f32(c, p, st);

@@ -1,8 +1,11 @@
 // rows_launch.cuh -- host-side launch of the row kernels for one Op policy.
 #pragma once
 
+#include <atomic>
+
 #include "launch.h"
 #include "rows.cuh"
+#include "rows_pipe.cuh"
 
 namespace b200norm {
 
@@ -64,9 +67,49 @@ RowsKernelFn<Op> pick_cta_kernel(int nv) {
   }
 }
 
+// The pipelined schedule: one CTA per SM, at most one per tile.
+template <class Op>
+cudaError_t launch_pipe(const typename Op::Args& a, const RowPlan& p, int nvec,
+                        cudaStream_t stream) {
+  void (*fn)(const typename Op::Args, int, int, unsigned long long, unsigned*, int) =
+      rows_pipe_kernel<Op>;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // the ring is larger than the default dynamic shared-memory limit: raise
+  // it once per device
+  static std::atomic<unsigned long long> raised{0};
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(raised.load() & bit)) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kPipeSmemBytes));
+    if (e != cudaSuccess) return e;
+    raised.fetch_or(bit);
+  }
+  unsigned* status = pipe_status_word();
+  if (!status) return cudaErrorSymbolNotFound;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.stream = stream;
+  const int64_t resident = static_cast<int64_t>(sms) * kPipeMinBlocks;
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid < resident ? p.grid : resident));
+  cfg.blockDim = dim3(kPipeThreads);
+  cfg.dynamicSmemBytes = kPipeSmemBytes;
+  cfg.attrs = attr;
+  cfg.numAttrs = add_pdl_attr(attr, 0);
+  const bool stall = pipe_stalled();
+  return cudaLaunchKernelEx(&cfg, fn, a, p.tpr, nvec, stall ? pipe_stall_limit_ns() : kPipeLimitNs,
+                            status, stall ? 1 : 0);
+}
+
 template <class Op>
 cudaError_t launch_rows_op(const typename Op::Args& a, const RowPlan& p, cudaStream_t stream) {
   const int nvec = static_cast<int>(a.n / p.ve);
+  if (p.mode == 3) {
+    if constexpr (sizeof(typename Op::P) == 16) return launch_pipe<Op>(a, p, nvec, stream);
+    return cudaErrorInvalidConfiguration;
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   cfg.stream = stream;

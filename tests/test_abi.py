@@ -194,10 +194,17 @@ def test_row_planner_shapes(lib):
 
 
 def test_force_hook_validation(lib):
-    assert lib.b200norm_testing_force(1, 0) == INVALID
+    assert lib.b200norm_testing_force(-1, 0) == INVALID
+    assert lib.b200norm_testing_force(1, 0) == OK
     assert lib.b200norm_testing_force(0, 1) == INVALID
     assert lib.b200norm_testing_force(0, 5) == INVALID
+    assert lib.b200norm_testing_force(4, 0) == INVALID
+    assert lib.b200norm_testing_force(3, 0) == OK
     assert lib.b200norm_testing_force(0, 0) == OK
+    assert lib.b200norm_testing_pipe_stall(2, 1000) == INVALID
+    assert lib.b200norm_testing_pipe_stall(1, 0) == INVALID
+    assert lib.b200norm_testing_pipe_stall(1, 6_000_000_000) == INVALID
+    assert lib.b200norm_testing_pipe_stall(0, 0) == OK
     for bad in ((3, 1), (2, 3), (0, 1), (32, 1), (1, 16)):
         assert lib.b200norm_testing_force_split(*bad) == INVALID, bad
     assert lib.b200norm_testing_force_split(16, 8) == OK

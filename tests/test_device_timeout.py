@@ -83,3 +83,32 @@ def test_workspace_left_ready_after_many_calls():
         ry, _ = oracle.skip_group(d["x"], d["skip"], d["gamma"], d["beta"], d["bias"], groups=G,
                                   activation=1, channels_last=1)
         assert_y_close(to_host(y), ry)
+
+
+def test_pipelined_rows_stall_reports_timeout_and_recovers():
+    """The pipelined row schedule's waits are bounded: with its producer
+    stalled (no copy is issued, so no tile ever lands) every consumer gives up
+    after the limit, the status call reports the timeout once and clears it,
+    and the next normal launch is correct."""
+    lib = b2.library()
+    d = synthetic.gated_rms_inputs((40000, 128), 128, np.float16, seed=2)
+    x, g, sc = (to_dev(d[k]) for k in ("x", "gate", "scale"))
+    assert lib.b200norm_testing_force(3, 0) == 0
+    try:
+        assert lib.b200norm_testing_pipe_stall(1, 20_000_000) == 0
+        t0 = time.time()
+        b2.gated_rms(x, g, sc, epsilon=1e-5)
+        with pytest.raises(b2.B200NormError) as e:
+            b2.rows_status()
+        assert e.value.status == TIMEOUT
+        assert time.time() - t0 < 10.0
+        b2.rows_status()  # the record was cleared
+    finally:
+        lib.b200norm_testing_pipe_stall(0, 0)
+    try:
+        y = b2.gated_rms(x, g, sc, epsilon=1e-5)
+        b2.rows_status()
+    finally:
+        lib.b200norm_testing_force(0, 0)
+    ry = oracle.gated_rms(d["x"], d["gate"], d["scale"], epsilon=1e-5)
+    assert_y_close(to_host(y), ry)
