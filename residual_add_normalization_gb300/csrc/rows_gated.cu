@@ -116,14 +116,14 @@ static std::atomic<bool> g_pipe_stall{false};
 static std::atomic<unsigned long long> g_pipe_stall_limit_ns{kPipeLimitNs};
 
 unsigned* pipe_status_word() {
-  constexpr int kMaxDevices = 64;
-  static std::atomic<unsigned*> cache[kMaxDevices];
+  constexpr int kCachedDevices = 64;  // devices past these are looked up every time
+  static std::atomic<unsigned*> cache[kCachedDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
     cudaGetLastError();
     return nullptr;
   }
-  unsigned* p = cache[dev].load();
+  unsigned* p = dev < kCachedDevices ? cache[dev].load() : nullptr;
   if (p) return p;
   void* addr = nullptr;
   if (cudaGetSymbolAddress(&addr, g_pipe_status) != cudaSuccess) {
@@ -131,7 +131,7 @@ unsigned* pipe_status_word() {
     return nullptr;
   }
   p = static_cast<unsigned*>(addr);
-  cache[dev].store(p);
+  if (dev < kCachedDevices) cache[dev].store(p);
   return p;
 }
 

@@ -78,10 +78,10 @@ cudaError_t launch_pipe(const typename Op::Args& a, const RowPlan& p, int nvec,
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   // the ring is larger than the default dynamic shared-memory limit: raise
-  // it once per device
+  // it once per device (every time on devices past the first 64)
   static std::atomic<unsigned long long> raised{0};
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(raised.load() & bit)) {
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (!bit || !(raised.load() & bit)) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kPipeSmemBytes));
     if (e != cudaSuccess) return e;
