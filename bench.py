@@ -224,26 +224,31 @@ def op_graphs_of(torch, calls, stream):
 
 
 def time_op_graphs(torch, graphs, reps, rounds, stream):
-    """Milliseconds per call of each workload: CUDA events around `rounds`
-    replays of its graph (after one untimed replay)."""
-    out = np.zeros(len(graphs))
-    for i, (g, rep) in enumerate(zip(graphs, reps)):
+    """Milliseconds per call of each workload over `rounds` back-to-back
+    replays of its graph (after one untimed replay), with an event between
+    consecutive replays: (mean, median, best) per workload.  The mean is the
+    whole run's time over its calls."""
+    out = []
+    for g, rep in zip(graphs, reps):
         g.replay()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(rounds):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(rounds + 1)]
+        ev[0].record(stream)
+        for k in range(rounds):
             g.replay()
-        e1.record(stream)
+            ev[k + 1].record(stream)
         torch.cuda.synchronize()
-        out[i] = e0.elapsed_time(e1) / (rounds * rep)
+        per = np.array([ev[k].elapsed_time(ev[k + 1]) / rep for k in range(rounds)])
+        out.append((ev[0].elapsed_time(ev[rounds]) / (rounds * rep), float(np.median(per)),
+                    float(per.min())))
     return out
 
 
-def op_entry(c, ms):
+def op_entry(c, t):
+    ms, med, best = t
     peak, _ = peak_hbm()
     gbs = c["bytes"] / (ms * 1e-3) / 1e9
-    return {"us_per_call": round(ms * 1e3, 3), "GB_s": round(gbs, 1),
+    return {"us_per_call": round(ms * 1e3, 3), "us_per_call_median": round(med * 1e3, 3),
+            "us_per_call_best": round(best * 1e3, 3), "GB_s": round(gbs, 1),
             "frac_of_measured_peak": round(gbs / peak, 4),
             "frac_of_8TBs_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
             "units_per_s": round(c["units"] / (ms * 1e-3), 1),
@@ -450,9 +455,10 @@ def run_ours(args, rank, world, dist):
     value = job_gbs(step_bytes, world, ms_per_step)
     peak, peak_src = peak_hbm()
     per_op = {c["name"]: op_entry(c, ms) for c, ms in zip(calls, per_call_ms)}
-    dom = int(np.argmax(per_call_ms))
+    mean_ms = [t[0] for t in per_call_ms]
+    dom = int(np.argmax(mean_ms))
     dom_c = calls[dom]
-    achieved = dom_c["bytes"] / (per_call_ms[dom] * 1e-3) / 1e9
+    achieved = dom_c["bytes"] / (mean_ms[dom] * 1e-3) / 1e9
     digest = buildlib.source_digest()
     family = "group" if dom_c["spec"]["op"] == "skip_group" else "rows"
     traffic = NCU_TRAFFIC.get((dom_c["name"], buildlib.source_digest(family)))
