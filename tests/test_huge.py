@@ -59,6 +59,50 @@ def test_huge_gated_rms():
     assert_y_close(to_host(y[idx]), ry)
 
 
+def test_huge_skip_rms_pipelined():
+    """Short bfloat16 rows take the pipelined schedule automatically: tiles
+    and stores past 2^31 elements."""
+    hidden = 256
+    rows = -(-BIG // hidden)
+    if _free_gb() < 4 * rows * hidden * 2 / 1e9 + 4:
+        pytest.skip("not enough device memory")
+    x = synthetic.device_normal((rows, hidden), torch.bfloat16, 21, "cuda")
+    sk = synthetic.device_normal((rows, hidden), torch.bfloat16, 22, "cuda")
+    ga = synthetic.device_normal((hidden,), torch.bfloat16, 23, "cuda", 1.0, 0.1)
+    bi = synthetic.device_normal((hidden,), torch.bfloat16, 24, "cuda", 0.0, 0.1)
+    y, s = b2.skip_rms(x, sk, ga, bi, epsilon=1e-6)
+    b2.rows_status()
+    pick = np.unique(np.concatenate([[0, 1], np.linspace(2, rows - 3, 12).astype(np.int64),
+                                     [rows - 2, rows - 1]]))
+    idx = torch.from_numpy(pick).cuda()
+    ry, rs = oracle.skip_rms(to_host(x[idx]), to_host(sk[idx]), to_host(ga), to_host(bi),
+                             epsilon=1e-6)
+    assert_bitexact(to_host(s[idx]), rs)
+    assert_y_close(to_host(y[idx]), ry)
+
+
+def test_huge_gated_rms_pipelined():
+    """GatedRMSNorm through the pipelined schedule (forced) past 2^31 elements."""
+    C = 128
+    spans = -(-BIG // C)
+    if _free_gb() < 3 * spans * C * 2 / 1e9 + 4:
+        pytest.skip("not enough device memory")
+    x = synthetic.device_normal((spans, C), torch.float16, 25, "cuda")
+    g = synthetic.device_normal((spans, C), torch.float16, 26, "cuda")
+    sc = synthetic.device_normal((C,), torch.float16, 27, "cuda", 1.0, 0.1)
+    assert b2.library().b200norm_testing_force(3, 0) == 0
+    try:
+        y = b2.gated_rms(x, g, sc)
+        b2.rows_status()
+    finally:
+        b2.library().b200norm_testing_force(0, 0)
+    pick = np.unique(np.concatenate([[0], np.linspace(1, spans - 2, 14).astype(np.int64),
+                                     [spans - 1]]))
+    idx = torch.from_numpy(pick).cuda()
+    ry = oracle.gated_rms(to_host(x[idx]), to_host(g[idx]), to_host(sc), epsilon=1e-5)
+    assert_y_close(to_host(y[idx]), ry)
+
+
 @pytest.mark.parametrize("cl", [0, 1])
 def test_huge_skip_group(cl):
     N, C, groups = 1, 256, 32
