@@ -33,6 +33,8 @@ B200NORM_API b200norm_status b200norm_testing_barrier_timeout(void* workspace,
  *   group_route: 2 = NHWC cooperative grid with one bounded grid barrier
  *                3 = two-phase partials -> normalize (any shape)
  *                4 = NHWC through L2 (statistics kernel, then apply kernel)
+ *                5 = NHWC through L2 in one cooperative grid (statistics, a
+ *                    bounded grid barrier, then a second pass over L2)
  * Other values are rejected with B200NORM_ERR_INVALID_ARGUMENT.  A later
  * SkipGroupNorm call that the forced route cannot take returns
  * B200NORM_ERR_UNSUPPORTED. */

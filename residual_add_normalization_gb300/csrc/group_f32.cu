@@ -16,6 +16,12 @@ void* group_resident_kernel_f32(DType m, int ve) {
   return nullptr;
 }
 
+void* group_coop_l2_kernel_f32(DType m, int ve, bool bcast) {
+  if (m == DType::F32) return pick_coop_l2<float, float>(ve, bcast);
+  if (m == DType::F16) return pick_coop_l2<float, __half>(ve, bcast);
+  return nullptr;
+}
+
 cudaError_t launch_group_f32(const SkipGroupCall& c, const GroupPlan& p, cudaStream_t stream) {
   if (c.m == DType::F32) return launch_group_typed<float, float>(c, p, stream);
   if (c.m == DType::F16) return launch_group_typed<float, __half>(c, p, stream);

@@ -458,26 +458,28 @@ constexpr int kL2Passes = 2;       // pixels per thread in flight
 constexpr int kL2MaxThreads = 512;
 constexpr int64_t kL2RouteMaxBytes = 48ll << 20;  // re-read through the 129 MB L2
 
+// Shared memory of the per-CTA statistics: per-thread sums [2][VE][PL][CV],
+// later the merge slices [3][S][groups].
+template <int VE>
+__host__ __device__ constexpr int nhwc_red_floats() {
+  return 2 * kL2MaxThreads * VE > 3 * 1024 ? 2 * kL2MaxThreads * VE : 3 * 1024;
+}
+
+// One CTA's statistics over pixels [p0, p1) of batch item n (routes 4 and 5):
+// K[g] into s_K, then per group the sums of S - K[g] and (S - K[g])^2 and the
+// element count, written to part[b * groups + g] as (sum, sum of squares,
+// count, 0).  X and skip are read with the default cache policy, so that the
+// second pass finds them in L2.  Every thread of the CTA calls it; it ends
+// with the partial stores issued (no barrier after them).
 template <typename T, typename M, int VE, bool BC>
-__global__ void __launch_bounds__(kL2MaxThreads, 2)
-sgn_nhwc_stats(const SgnArgs<T, M> a, int B, int ppc) {
-  pdl_wait();
-  pdl_trigger();
-  // s_red: per-thread sums [2][VE][PL][CV], later the merge slices [3][S][groups]
-  constexpr int kRed = 2 * kL2MaxThreads * VE > 3 * 1024 ? 2 * kL2MaxThreads * VE : 3 * 1024;
-  __shared__ float s_red[kRed];
-  __shared__ float s_col[2 * 1024];  // [2][C], C <= 1024
-  __shared__ unsigned s_last;
-  extern __shared__ float s_K[];  // [groups]
+__device__ __forceinline__ void nhwc_partials(const SgnArgs<T, M>& a, int n, int b, int p0,
+                                              int p1, float* s_K, float* s_red, float* s_col,
+                                              float4* part) {
   const int C = a.C;
   const int CV = C / VE;
   const int PL = blockDim.x / CV;
   const int tc = threadIdx.x % CV;
   const int tp = threadIdx.x / CV;
-  const int n = blockIdx.x / B;
-  const int b = blockIdx.x % B;
-  const int p0 = b * ppc;
-  const int p1 = min(p0 + ppc, a.HW);
   const int64_t nbase = static_cast<int64_t>(n) * a.HW * C;
   const int c0 = tc * VE;
   const bool active = tp < PL;
@@ -545,7 +547,6 @@ sgn_nhwc_stats(const SgnArgs<T, M> a, int B, int ppc) {
   }
   __syncthreads();
   const float cnt = static_cast<float>(p1 - p0) * static_cast<float>(a.cpg);
-  float4* part = a.part + static_cast<int64_t>(n) * B * a.groups;
   for (int g = threadIdx.x; g < a.groups; g += blockDim.x) {
     float t1 = 0.0f, t2 = 0.0f;
     for (int cc = 0; cc < a.cpg; ++cc) {
@@ -554,25 +555,17 @@ sgn_nhwc_stats(const SgnArgs<T, M> a, int B, int ppc) {
     }
     part[static_cast<int64_t>(b) * a.groups + g] = make_float4(t1, t2, cnt, 0.0f);
   }
-  // The last CTA of this batch item merges its partials.  The barrier orders
-  // every thread's partial stores before thread 0's fence, and the fence
-  // (cumulative) makes them visible GPU-wide before the count goes up; on
-  // the merging side the fence after the count orders the reads after it.
-  __syncthreads();
-  float4* stats = a.part + a.N * B * a.groups;
-  unsigned* counter = a.ctl->item_done + n;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_last = atomicAdd(counter, 1u) == static_cast<unsigned>(B - 1);
-    if (s_last) __threadfence();
-  }
-  __syncthreads();
-  if (!s_last) return;
-  // Slice j of group g adds partials j, j + S, j + 2S, ... (S slices per
-  // group, the block's threads spread over groups x slices); the slices are
-  // then added in order, so the result does not depend on which CTA merges.
+}
+
+// Adds a batch item's B partials per group in a fixed order: slice j of group
+// g adds partials j, j + S, j + 2S, ... (S slices per group, the block's
+// threads spread over groups x slices), then the slices are added in order,
+// so every CTA that merges gets the same bits.  Leaves (d, rstd) of group g in
+// s_out[g] and s_out[groups + g]; ends with a barrier.
+template <typename T, typename M>
+__device__ __forceinline__ void nhwc_merge(const SgnArgs<T, M>& a, const float4* part, int B,
+                                           float* s_m, float* s_out) {
   const int S = max(1, static_cast<int>(blockDim.x) / a.groups);
-  float* s_m = s_red;  // [3][S][groups]
   for (int idx = threadIdx.x; idx < S * a.groups; idx += blockDim.x) {
     const int g = idx % a.groups, j = idx / a.groups;
     float t1 = 0.0f, t2 = 0.0f, c = 0.0f;
@@ -608,9 +601,45 @@ sgn_nhwc_stats(const SgnArgs<T, M> a, int B, int ppc) {
     }
     const float d = t1 / c;
     const float var = fmaxf(t2 / c - d * d, 0.0f);
-    stats[static_cast<int64_t>(n) * a.groups + g] =
-        make_float4(s_K[g], d, 1.0f / sqrtf(var + a.eps), 0.0f);
+    s_out[g] = d;
+    s_out[a.groups + g] = 1.0f / sqrtf(var + a.eps);
   }
+  __syncthreads();
+}
+
+template <typename T, typename M, int VE, bool BC>
+__global__ void __launch_bounds__(kL2MaxThreads, 2)
+sgn_nhwc_stats(const SgnArgs<T, M> a, int B, int ppc) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float s_red[nhwc_red_floats<VE>()];
+  __shared__ float s_col[2 * 1024];  // [2][C], C <= 1024
+  __shared__ unsigned s_last;
+  extern __shared__ float s_K[];  // [groups]
+  const int n = blockIdx.x / B;
+  const int b = blockIdx.x % B;
+  const int p0 = b * ppc;
+  const int p1 = min(p0 + ppc, a.HW);
+  float4* part = a.part + static_cast<int64_t>(n) * B * a.groups;
+  nhwc_partials<T, M, VE, BC>(a, n, b, p0, p1, s_K, s_red, s_col, part);
+  // The last CTA of this batch item merges its partials.  The barrier orders
+  // every thread's partial stores before thread 0's fence, and the fence
+  // (cumulative) makes them visible GPU-wide before the count goes up; on
+  // the merging side the fence after the count orders the reads after it.
+  __syncthreads();
+  float4* stats = a.part + a.N * B * a.groups;
+  unsigned* counter = a.ctl->item_done + n;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(counter, 1u) == static_cast<unsigned>(B - 1);
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+  nhwc_merge(a, part, B, s_red, s_col);
+  for (int g = threadIdx.x; g < a.groups; g += blockDim.x)
+    stats[static_cast<int64_t>(n) * a.groups + g] =
+        make_float4(s_K[g], s_col[g], s_col[a.groups + g], 0.0f);
   if (threadIdx.x == 0) *counter = 0u;  // ready for the next call
 }
 
@@ -689,6 +718,92 @@ sgn_nhwc_apply(const SgnArgs<T, M> a, int B, int ppc) {
       }
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Route 5: NHWC, one cooperative grid re-reading its inputs through L2
+// ---------------------------------------------------------------------------
+// Route 4's work in one launch: every CTA takes the statistics of its pixel
+// range (nhwc_partials), meets the grid at one bounded barrier, adds its
+// batch item's partials itself (nhwc_merge, the same order in every CTA),
+// turns them into the per-channel table (K, d, rstd * gamma[c], beta[c]) and
+// walks its pixel range again -- X and skip now come from L2 -- forming S and
+// writing S and Y.  No second launch, and no last-CTA merge that the rest of
+// the grid waits for.  Needs every CTA resident at once (a cooperative
+// launch) and the inputs to stay in L2 between the passes (as route 4).
+// Dynamic shared memory: table [C] float4 | K [groups] float.
+template <typename T, typename M, int VE, bool BC>
+__global__ void __launch_bounds__(kL2MaxThreads, 2)
+sgn_nhwc_coop_l2(const SgnArgs<T, M> a, int B, int ppc) {
+  __shared__ float s_red[nhwc_red_floats<VE>()];
+  __shared__ float s_col[2 * 1024];  // [2][C], C <= 1024; then (d, rstd) per group
+  extern __shared__ float4 s_dyn[];
+  float4* s_coef = s_dyn;
+  float* s_K = reinterpret_cast<float*>(s_dyn + a.C);
+  const int C = a.C;
+  const int CV = C / VE;
+  const int PL = blockDim.x / CV;
+  const int tc = threadIdx.x % CV;
+  const int tp = threadIdx.x / CV;
+  const int n = blockIdx.x / B;
+  const int b = blockIdx.x % B;
+  const int p0 = b * ppc;
+  const int p1 = min(p0 + ppc, a.HW);
+  const int64_t nbase = static_cast<int64_t>(n) * a.HW * C;
+  const int c0 = tc * VE;
+  float4* part = a.part + static_cast<int64_t>(n) * B * a.groups;
+
+  nhwc_partials<T, M, VE, BC>(a, n, b, p0, p1, s_K, s_red, s_col, part);
+  // the arrival's release (after a CTA barrier) publishes the partials
+  grid_arrive(a.ctl);
+  unsigned departure = 0u;
+  if (!grid_wait(a.ctl, gridDim.x, a.limit_ns, 5u, departure)) {
+    grid_depart(a.ctl, departure);
+    return;
+  }
+  nhwc_merge(a, part, B, s_red, s_col);
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    const int g = c / a.cpg;
+    s_coef[(c % VE) * CV + c / VE] =
+        make_float4(s_K[g], s_col[g], s_col[a.groups + g] * to_f32(__ldg(a.gamma + c)),
+                    to_f32(__ldg(a.beta + c)));
+  }
+  __syncthreads();
+  if (tp < PL) {
+    Pack<T, VE> skb, bv;
+    if constexpr (BC) skb = ld_reuse<T, VE>(a.skip + static_cast<int64_t>(n) * C + c0);
+    if (a.bias) bv = ld_reuse<T, VE>(a.bias + c0);
+    for (int q = p0 + tp; q < p1; q += kL2Passes * PL) {
+      Pack<T, VE> xv[kL2Passes], kv[BC ? 1 : kL2Passes];
+#pragma unroll
+      for (int k = 0; k < kL2Passes; ++k) {
+        const int p = q + k * PL;
+        if (p < p1) {
+          const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+          xv[k] = ld_stream<T, VE>(a.x + off);
+          if constexpr (!BC) kv[k] = ld_stream<T, VE>(a.skip + off);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kL2Passes; ++k) {
+        const int p = q + k * PL;
+        if (p < p1) {
+          const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+          Pack<T, VE> sv, out;
+#pragma unroll
+          for (int e = 0; e < VE; ++e) {
+            const float sk = BC ? to_f32(skb.v[e]) : to_f32(kv[BC ? 0 : k].v[e]);
+            sv.v[e] = sgn_sum_b<T>(to_f32(xv[k].v[e]), sk, to_f32(bv.v[e]), a.bias != nullptr);
+            const float4 cf = s_coef[e * CV + tc];
+            out.v[e] = from_f32<T>(sgn_out(to_f32(sv.v[e]), cf.x, cf.y, cf.z, 1.0f, cf.w, a.act));
+          }
+          if (a.s) st_stream<T, VE>(a.s + off, sv);
+          st_stream<T, VE>(a.y + off, out);
+        }
+      }
+    }
+  }
+  grid_depart(a.ctl, departure);
 }
 
 // ---------------------------------------------------------------------------
@@ -891,6 +1006,16 @@ inline void pick_l2_ve(bool bcast, void** stats, void** apply) {
 }
 
 template <typename T, typename M>
+inline void* pick_coop_l2(int ve, bool bcast) {
+  constexpr int V16 = static_cast<int>(16 / sizeof(T));
+  if (ve == 1)
+    return bcast ? reinterpret_cast<void*>(sgn_nhwc_coop_l2<T, M, 1, true>)
+                 : reinterpret_cast<void*>(sgn_nhwc_coop_l2<T, M, 1, false>);
+  return bcast ? reinterpret_cast<void*>(sgn_nhwc_coop_l2<T, M, V16, true>)
+               : reinterpret_cast<void*>(sgn_nhwc_coop_l2<T, M, V16, false>);
+}
+
+template <typename T, typename M>
 inline void pick_l2(int ve, bool bcast, void** stats, void** apply) {
   constexpr int V16 = static_cast<int>(16 / sizeof(T));
   if (ve == 1) pick_l2_ve<T, M, 1>(bcast, stats, apply);
@@ -959,6 +1084,17 @@ inline cudaError_t launch_group_typed(const SkipGroupCall& c, const GroupPlan& p
     void* args[] = {&a, &B, &ppc, &koff};
     return cudaLaunchKernelExC(&cfg, fn, args);
   }
+  if (p.route == 5) {
+    // A cooperative launch keeps plain stream order (no early scheduling).
+    void* fn = pick_coop_l2<T, M>(p.ve, c.bcast);
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int B = p.ctas_per_item, ppc = p.pix_per_cta;
+    void* args[] = {&a, &B, &ppc};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+  }
   if (p.route == 4) {
     void *stats = nullptr, *apply = nullptr;
     pick_l2<T, M>(p.ve, c.bcast, &stats, &apply);
@@ -995,6 +1131,9 @@ void* group_coop_kernel_bf16(DType m, int ve, int nv);
 void* group_resident_kernel_f32(DType m, int ve);
 void* group_resident_kernel_f16(DType m, int ve);
 void* group_resident_kernel_bf16(DType m, int ve);
+void* group_coop_l2_kernel_f32(DType m, int ve, bool bcast);
+void* group_coop_l2_kernel_f16(DType m, int ve, bool bcast);
+void* group_coop_l2_kernel_bf16(DType m, int ve, bool bcast);
 cudaError_t launch_group_f32(const SkipGroupCall& c, const GroupPlan& p, cudaStream_t stream);
 cudaError_t launch_group_f16(const SkipGroupCall& c, const GroupPlan& p, cudaStream_t stream);
 cudaError_t launch_group_bf16(const SkipGroupCall& c, const GroupPlan& p, cudaStream_t stream);

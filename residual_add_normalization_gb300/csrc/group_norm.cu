@@ -67,6 +67,15 @@ static void* pick_resident_any(DType t, DType m, int ve) {
   return nullptr;
 }
 
+static void* pick_coop_l2_any(DType t, DType m, int ve, bool bcast) {
+  switch (t) {
+    case DType::F32: return group_coop_l2_kernel_f32(m, ve, bcast);
+    case DType::F16: return group_coop_l2_kernel_f16(m, ve, bcast);
+    case DType::BF16: return group_coop_l2_kernel_bf16(m, ve, bcast);
+  }
+  return nullptr;
+}
+
 static bool resident_cluster_fits(void* fn, int block, int csize, size_t smem) {
   if (csize > 8 &&
       cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
@@ -169,6 +178,52 @@ static bool plan_l2_route(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) 
   return true;
 }
 
+// Route 5: route 4's passes in one cooperative grid.  Same shape limits as
+// route 4 except the batch-item count (it keeps no per-item counters): every
+// CTA must be resident at once, at most kMaxCoopCtas of them.
+static bool plan_coop_l2_route(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) {
+  if (!c.channels_last) return false;
+  const int64_t es = static_cast<int64_t>(dtype_size(c.t));
+  const int vec = static_cast<int>(16 / es);
+  const int ve = (vector_ok && c.C % vec == 0) ? vec : 1;
+  const int64_t numel = c.N * c.H * c.W * c.C;
+  if (!l2_route_ok(1, c.C, ve, numel * es * (c.bcast ? 1 : 2))) return false;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  void* fn = pick_coop_l2_any(c.t, c.m, ve, c.bcast);
+  const int64_t HW = c.H * c.W;
+  const int PL = static_cast<int>(kL2MaxThreads / (c.C / ve));
+  const int block = static_cast<int>(PL * (c.C / ve));
+  const size_t smem = static_cast<size_t>(c.C) * sizeof(float4) +
+                      static_cast<size_t>(c.groups) * sizeof(float);
+  int per_sm = 0;
+  if (!fn || !allow_smem(fn, smem, dev) ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, block, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  const int64_t cap = std::min<int64_t>(static_cast<int64_t>(per_sm) * sms, kMaxCoopCtas);
+  if (c.N > cap) return false;
+  int64_t B = std::min<int64_t>(cdiv(HW, PL), cap / c.N);
+  const int64_t ppc = cdiv(HW, B);
+  B = cdiv(HW, ppc);
+  *p = GroupPlan{};
+  p->route = 5;
+  p->ve = ve;
+  p->nv = kL2Passes;
+  p->block = block;
+  p->csize = 1;
+  p->grid = c.N * B;
+  p->ctas_per_item = static_cast<int>(B);
+  p->pix_per_cta = static_cast<int>(ppc);
+  p->smem = smem;
+  return true;
+}
+
 static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, int force,
                                        GroupPlan* p);
 
@@ -217,12 +272,16 @@ static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, i
     return cudaSuccess;
   }
   if (force == 4) return plan_l2_route(c, vector_ok, p) ? cudaSuccess : cudaErrorNotSupported;
+  if (force == 5) return plan_coop_l2_route(c, vector_ok, p) ? cudaSuccess : cudaErrorNotSupported;
   if (force == 0 && c.channels_last) {
-    // NHWC: the cooperative route whenever its grid can be resident, else the
-    // L2 route, else two-phase.  (Measured on GB300: (2, 64, 64, 320) fp16
-    // 11.6 us cooperative vs 16.2 us through L2; (1, 128, 128, 128) fp16
-    // 11.3 vs 11.9 us; (8, 32, 32, 512) fp16 13.5 vs 16.4 us.)
+    // NHWC: the cooperative route whenever its grid can hold the pixels in
+    // registers, else one cooperative grid re-reading through L2, else the
+    // two-kernel L2 route, else two-phase.  (Measured on GB300: (2, 64, 64,
+    // 320) fp16 9.9 us cooperative vs 13.3 / 13.5 us through L2 in one grid /
+    // two kernels; (4, 64, 64, 320) fp16 16.8 vs 17.5 us and fp32 (2, 64, 64,
+    // 320) 13.9 vs 15.2 us through L2 in one grid vs two kernels.)
     if (plan_group_uncached(c, vector_ok, 2, p) == cudaSuccess) return cudaSuccess;
+    if (plan_coop_l2_route(c, vector_ok, p)) return cudaSuccess;
     if (plan_l2_route(c, vector_ok, p)) return cudaSuccess;
     *p = two_phase_plan(c);
     return cudaSuccess;

@@ -157,13 +157,14 @@ struct GroupPlan {
                   // 2: NHWC cooperative (grid barrier)
                   // 3: two-phase partials -> normalize (any shape)
                   // 4: NHWC through L2 (statistics kernel, then apply kernel)
+                  // 5: NHWC through L2 in one cooperative grid (grid barrier)
   int ve;         // elements per vector access, or 1
   int nv;         // vectors held per thread
   int block;      // threads per CTA
   int csize;      // CTAs per cluster (route 1)
   int64_t grid;   // CTAs
-  int ctas_per_item;   // routes 2, 4: CTAs per batch item
-  int pix_per_cta;     // routes 2, 4: pixels per CTA
+  int ctas_per_item;   // routes 2, 4, 5: CTAs per batch item
+  int pix_per_cta;     // routes 2, 4, 5: pixels per CTA
   int chunks;          // route 3: chunks per group instance
   size_t smem;         // dynamic shared memory bytes
 };

@@ -104,6 +104,7 @@ NHWC_CASES = [
     (2, 64, 64, 96, 24),    # cpg 4: 8-channel vectors span two groups
     (64, 8, 8, 64, 8),      # 64 batch items: the cooperative route
     (1, 128, 128, 128, 32), # one item over every SM, 32 groups
+    (64, 32, 32, 320, 32),  # 64 items, too many pixels for registers: one grid through L2
 ]
 
 
@@ -128,12 +129,13 @@ def test_forced_two_phase(cl, dtype):
     check(d, 8, 1, cl)
 
 
-@pytest.mark.parametrize("route", [2, 4])
+@pytest.mark.parametrize("route", [2, 4, 5])
 @pytest.mark.parametrize("dtype,mdtype", TYPE_PAIRS)
 @pytest.mark.parametrize("case", NHWC_CASES)
 def test_nhwc_forced_routes(route, dtype, mdtype, case):
-    """Both NHWC routes on every NHWC case they can take (the planner picks
-    route 4 for tensors that stay in L2 and route 2 for larger ones)."""
+    """The NHWC routes 2, 4 and 5 on every NHWC case each can take (route 2
+    holds a resident grid's pixels in registers; routes 4 and 5 re-read
+    tensors that stay in L2, in two launches or in one cooperative grid)."""
     N, H, W, C, G = case
     assert b2.library().b200norm_testing_force(0, route) == 0
     for skip, bias, act, want_sum in (("nc", True, 1, True), ("full", False, 0, False)):
@@ -154,12 +156,16 @@ def test_route_coverage():
         routes.add((p["route"], p["csize"] > 1))
     for N, H, W, C, G in NHWC_CASES:
         routes.add((plan((N, H, W, C), G, np.float16, np.float32, 1)["route"], False))
-    assert {r for r, _ in routes} == {1, 2, 3}
+    assert {1, 2, 3} <= {r for r, _ in routes} <= {1, 2, 3, 5}
     assert (1, True) in routes, "no cluster-per-instance case"
-    # the cooperative route while its grid can be resident, else through L2
+    # the cooperative route while its grid can hold the pixels in registers,
+    # else one cooperative grid through L2 (also for more batch items than the
+    # two-kernel L2 route counts)
     assert plan((2, 64, 64, 320), 32, np.float16, np.float32, 1)["route"] == 2
     assert plan((64, 8, 8, 64), 8, np.float16, np.float32, 1)["route"] == 2
-    assert plan((4, 64, 64, 320), 32, np.float16, np.float32, 1)["route"] == 4
+    assert plan((4, 64, 64, 320), 32, np.float16, np.float32, 1)["route"] == 5
+    assert plan((2, 128, 128, 320), 32, np.float16, np.float32, 1)["route"] == 5
+    assert plan((64, 24, 24, 320), 32, np.float16, np.float32, 1)["route"] == 5
 
 
 def test_n11c_at_hw1_equals_nc_route():
@@ -209,7 +215,9 @@ def test_one_workspace_serves_every_route_in_turn():
     calls = [((2, 64, 64, 320), 1, 32, None), ((1, 128, 128, 128), 1, 32, None),
              ((5, 16, 16, 64), 1, 8, 4), ((2, 64, 16, 16), 0, 8, None),
              ((1, 128, 128, 128), 1, 32, None), ((3, 16, 16, 96), 1, 12, 3),
-             ((2, 64, 64, 320), 1, 32, 4), ((64, 8, 8, 64), 1, 8, None)]
+             ((2, 64, 64, 320), 1, 32, 4), ((64, 8, 8, 64), 1, 8, None),
+             ((4, 32, 32, 320), 1, 32, 5), ((1, 128, 128, 128), 1, 32, 5),
+             ((2, 64, 64, 320), 1, 32, None)]
     need = max(b2.workspace_size(*(s[0], s[3], s[1], s[2]) if cl else s, g, torch.float16, cl)
                for s, cl, g, _ in calls)
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
