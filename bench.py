@@ -42,6 +42,8 @@ DECODE_WORKLOADS = ["ssln_fp16_decode_1x4096", "ssln_fp16_decode_64x4096",
 # bfloat16 variants of the large workloads, timed like the step workloads.
 BF16_WORKLOADS = ["ssln_bf16_8x2048x4096", "gated_bf16_4x4096x8192_c128",
                   "sgn_nhwc_bf16_2x64x64x320", "sgn_nchw_bf16_16x1280x16x16"]
+# short SkipSimplifiedLayerNormalization rows: the pipelined bulk-copy schedule
+SHORT_WORKLOADS = ["ssln_fp32_262144x128"]
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -358,6 +360,21 @@ def run_ours(args, rank, world, dist):
         del graphs, bcalls
         torch.cuda.synchronize()
 
+    # --- short rows (the pipelined schedule), timed the same way -------------
+    short_ops = {}
+    if not args.no_short:
+        scalls = make_calls(torch, b2, dev, SHORT_WORKLOADS)
+        for c in scalls:
+            for f in c["fns"]:
+                f()
+        torch.cuda.synchronize()
+        graphs, sreps = op_graphs_of(torch, scalls, cap)
+        sms_ = time_op_graphs(torch, graphs, sreps, op_rounds, stream)
+        short_ops = {c["name"]: op_entry(c, ms) for c, ms in zip(scalls, sms_)}
+        del graphs, scalls
+        torch.cuda.synchronize()
+        b2.rows_status()
+
     # --- decode-shaped calls: per-call time in a graph of back-to-back calls -
     decode = {}
     if not args.no_decode:
@@ -481,6 +498,9 @@ def run_ours(args, rank, world, dist):
         "per_op": per_op,
         "per_op_bf16": ({"timing": "as per_op; bfloat16 storage, same shapes; not part of "
                                    "`value`", **bf16_ops} if bf16_ops else None),
+        "per_op_short_rows": ({"timing": "as per_op; short rows, which take the pipelined "
+                                          "bulk-copy schedule; not part of `value`",
+                               **short_ops} if short_ops else None),
         "decode": ({"timing": "best of 5 replays of a CUDA graph of 200 back-to-back calls on "
                               "one buffer set (inputs L2-resident, as when a preceding kernel "
                               "has just written them); not part of `value`",
@@ -620,12 +640,15 @@ def main():
                     help="skip the bfloat16 per-operator measurements")
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the decode-shaped latency measurements")
-    ap.add_argument("--only", choices=STEP_WORKLOADS + BF16_WORKLOADS + DECODE_WORKLOADS,
+    ap.add_argument("--no-short", action="store_true",
+                    help="skip the short-row (pipelined schedule) measurement")
+    ap.add_argument("--only", choices=STEP_WORKLOADS + BF16_WORKLOADS + DECODE_WORKLOADS +
+                    SHORT_WORKLOADS,
                     help="run a single workload (for profiler runs; not a bench line)")
     args = ap.parse_args()
     if args.only:
         STEP_WORKLOADS[:] = [args.only]
-        args.no_bf16 = args.no_decode = True
+        args.no_bf16 = args.no_decode = args.no_short = True
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -34,6 +34,10 @@ deviation ``s``.
   sgn_nhwc_bf16_2x64x64x320, sgn_nchw_bf16_16x1280x16x16  bfloat16 variants
                        of the large workloads (the NCHW one with bfloat16
                        gamma/beta); seeds 8-11.
+  ssln_fp32_262144x128  SkipSimplifiedLayerNormalization fp32 with short rows
+                       (262,144 rows of 128), distributions as
+                       ssln_fp16_8x2048x4096; seed 12 (the rows the pipelined
+                       bulk-copy schedule takes).
 
 bfloat16 host arrays are uint16 bit patterns whose dtype is ``BFLOAT16`` (a
 uint16 dtype carrying the metadata {"bfloat16": True}); values are drawn in
@@ -107,6 +111,9 @@ WORKLOADS = {
         op="skip_group", seed=11, dtype=BFLOAT16, mdtype=BFLOAT16,
         shape=(16, 1280, 16, 16), channels_last=0, skip="full", bias=False, x_std=2.0,
         groups=32, epsilon=1e-5, activation=0, want_sum=False),
+    "ssln_fp32_262144x128": dict(
+        op="skip_rms", seed=12, dtype=np.float32, shape=(262144, 128), bias=True,
+        gamma=("normal", 1.0, 0.1), epsilon=SSLN_EPS, want_sum=True),
 }
 
 # Order the workloads are listed in (small SSLN first, decode shapes last).
