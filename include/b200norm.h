@@ -73,7 +73,7 @@ typedef enum {
 typedef enum {
     B200NORM_OK = 0,
     B200NORM_ERR_INVALID_ARGUMENT = 1, /* bad pointer, shape, attribute or overlap   */
-    B200NORM_ERR_UNSUPPORTED = 2,      /* element type or shape this build refuses    */
+    B200NORM_ERR_UNSUPPORTED = 2,      /* element type or shape the library refuses   */
     B200NORM_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed        */
     B200NORM_ERR_WORKSPACE = 4,        /* SkipGroupNorm workspace missing / too small */
     B200NORM_ERR_DEVICE_TIMEOUT = 5    /* a device-side wait gave up (see below)      */
