@@ -235,3 +235,32 @@ def test_one_workspace_serves_every_route_in_turn():
         assert_bitexact(to_host(s), rs)
         assert_y_close(to_host(y), ry)
     b2.workspace_status(ws)
+
+
+@pytest.mark.parametrize("flag", [1, 2, 7, -1])
+def test_any_nonzero_channels_last_means_nhwc(flag):
+    """The C entry reads every non-zero channels_last as NHWC (SkipGroupNorm
+    README, Attributes, channels_last): raw calls with 1, 2, 7 and -1 give the
+    NHWC result bit for bit."""
+    shape, G = (2, 8, 8, 64), 8
+    d = synthetic.skip_group_inputs(shape, np.float16, np.float32, seed=17, channels_last=1,
+                                    skip="nc", bias=True)
+    x, sk, ga, be, bi = (to_dev(d[k]) for k in ("x", "skip", "gamma", "beta", "bias"))
+    N, H, W, C = shape
+    y = torch.empty_like(x)
+    s = torch.empty_like(x)
+    ws = torch.zeros(b2.workspace_size(N, C, H, W, G, torch.float16, 1), dtype=torch.uint8,
+                     device="cuda")
+    dims = (ctypes.c_int64 * 4)(N, C, 0, 0)
+    st = b2.library().b200norm_skip_group(
+        ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(sk.data_ptr()), 2, dims,
+        ctypes.c_void_p(bi.data_ptr()), ctypes.c_void_p(ga.data_ptr()),
+        ctypes.c_void_p(be.data_ptr()), ctypes.c_void_p(y.data_ptr()),
+        ctypes.c_void_p(s.data_ptr()), N, C, H, W, F16, F32, G, 1e-5, 1, flag,
+        ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    ry, rs = oracle.skip_group(d["x"], d["skip"], d["gamma"], d["beta"], d["bias"], groups=G,
+                               activation=1, channels_last=1)
+    assert_bitexact(to_host(s), rs)
+    assert_y_close(to_host(y), ry)
