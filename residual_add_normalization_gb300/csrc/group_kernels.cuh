@@ -569,23 +569,20 @@ __device__ __forceinline__ void nhwc_merge(const SgnArgs<T, M>& a, const float4*
   for (int idx = threadIdx.x; idx < S * a.groups; idx += blockDim.x) {
     const int g = idx % a.groups, j = idx / a.groups;
     float t1 = 0.0f, t2 = 0.0f, c = 0.0f;
-    int q = j;
-    for (; q + 7 * S < B; q += 8 * S) {
+    // eight loads in flight per batch; slots past B add +0, which leaves every
+    // sum's bits as they would be without them
+    for (int q = j; q < B; q += 8 * S) {
       float4 u[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) u[i] = __ldcg(part + static_cast<int64_t>(q + i * S) * a.groups + g);
+      for (int i = 0; i < 8; ++i)
+        u[i] = q + i * S < B ? __ldcg(part + static_cast<int64_t>(q + i * S) * a.groups + g)
+                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         t1 += u[i].x;
         t2 += u[i].y;
         c += u[i].z;
       }
-    }
-    for (; q < B; q += S) {
-      const float4 u = __ldcg(part + static_cast<int64_t>(q) * a.groups + g);
-      t1 += u.x;
-      t2 += u.y;
-      c += u.z;
     }
     s_m[(0 * S + j) * a.groups + g] = t1;
     s_m[(1 * S + j) * a.groups + g] = t2;
