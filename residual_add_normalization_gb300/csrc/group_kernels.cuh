@@ -455,6 +455,10 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
 // [N * B * groups] and the statistics [N * groups]; the control block holds
 // one counter per batch item (N <= kL2MaxItems), zero between calls.
 constexpr int kL2Passes = 2;       // pixels per thread in flight
+// the same in route 5: three (measured on GB300 against two and four: 1-3%
+// faster on (4, 64, 64, 320) / (2, 64, 64, 640) fp16 and (2, 64, 64, 320) fp32;
+// four spills more and is slower)
+constexpr int kCoopL2Passes = 3;
 constexpr int kL2MaxThreads = 512;
 constexpr int64_t kL2RouteMaxBytes = 48ll << 20;  // re-read through the 129 MB L2
 
@@ -471,7 +475,7 @@ __host__ __device__ constexpr int nhwc_red_floats() {
 // count, 0).  X and skip are read with the default cache policy, so that the
 // second pass finds them in L2.  Every thread of the CTA calls it; it ends
 // with the partial stores issued (no barrier after them).
-template <typename T, typename M, int VE, bool BC>
+template <typename T, typename M, int VE, bool BC, int PASSES = kL2Passes>
 __device__ __forceinline__ void nhwc_partials(const SgnArgs<T, M>& a, int n, int b, int p0,
                                               int p1, float* s_K, float* s_red, float* s_col,
                                               float4* part) {
@@ -498,10 +502,10 @@ __device__ __forceinline__ void nhwc_partials(const SgnArgs<T, M>& a, int n, int
     float Kl[VE];
 #pragma unroll
     for (int e = 0; e < VE; ++e) Kl[e] = s_K[(c0 + e) / a.cpg];
-    for (int q = p0 + tp; q < p1; q += kL2Passes * PL) {
-      Pack<T, VE> xv[kL2Passes], kv[BC ? 1 : kL2Passes];
+    for (int q = p0 + tp; q < p1; q += PASSES * PL) {
+      Pack<T, VE> xv[PASSES], kv[BC ? 1 : PASSES];
 #pragma unroll
-      for (int k = 0; k < kL2Passes; ++k) {
+      for (int k = 0; k < PASSES; ++k) {
         const int p = q + k * PL;
         if (p < p1) {
           const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
@@ -510,7 +514,7 @@ __device__ __forceinline__ void nhwc_partials(const SgnArgs<T, M>& a, int n, int
         }
       }
 #pragma unroll
-      for (int k = 0; k < kL2Passes; ++k) {
+      for (int k = 0; k < PASSES; ++k) {
         if (q + k * PL < p1) {
 #pragma unroll
           for (int e = 0; e < VE; ++e) {
@@ -750,7 +754,7 @@ sgn_nhwc_coop_l2(const SgnArgs<T, M> a, int B, int ppc) {
   const int c0 = tc * VE;
   float4* part = a.part + static_cast<int64_t>(n) * B * a.groups;
 
-  nhwc_partials<T, M, VE, BC>(a, n, b, p0, p1, s_K, s_red, s_col, part);
+  nhwc_partials<T, M, VE, BC, kCoopL2Passes>(a, n, b, p0, p1, s_K, s_red, s_col, part);
   // the arrival's release (after a CTA barrier) publishes the partials
   grid_arrive(a.ctl);
   unsigned departure = 0u;
@@ -770,10 +774,10 @@ sgn_nhwc_coop_l2(const SgnArgs<T, M> a, int B, int ppc) {
     Pack<T, VE> skb, bv;
     if constexpr (BC) skb = ld_reuse<T, VE>(a.skip + static_cast<int64_t>(n) * C + c0);
     if (a.bias) bv = ld_reuse<T, VE>(a.bias + c0);
-    for (int q = p0 + tp; q < p1; q += kL2Passes * PL) {
-      Pack<T, VE> xv[kL2Passes], kv[BC ? 1 : kL2Passes];
+    for (int q = p0 + tp; q < p1; q += kCoopL2Passes * PL) {
+      Pack<T, VE> xv[kCoopL2Passes], kv[BC ? 1 : kCoopL2Passes];
 #pragma unroll
-      for (int k = 0; k < kL2Passes; ++k) {
+      for (int k = 0; k < kCoopL2Passes; ++k) {
         const int p = q + k * PL;
         if (p < p1) {
           const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
@@ -782,7 +786,7 @@ sgn_nhwc_coop_l2(const SgnArgs<T, M> a, int B, int ppc) {
         }
       }
 #pragma unroll
-      for (int k = 0; k < kL2Passes; ++k) {
+      for (int k = 0; k < kCoopL2Passes; ++k) {
         const int p = q + k * PL;
         if (p < p1) {
           const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
