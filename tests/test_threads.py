@@ -23,7 +23,11 @@ def _work(seed):
                                      channels_last=1, skip="nc", bias=True)
     d4 = synthetic.skip_group_inputs((2, 320, 16, 16), np.float32, np.float16, seed=seed,
                                      channels_last=0, skip="full", bias=False)
-    t = [{k: to_dev(v) for k, v in d.items()} for d in (d1, d2, d3, d4)]
+    # NHWC too large for the register-resident cooperative route: one grid
+    # through L2 (route 5), also cooperative
+    d5 = synthetic.skip_group_inputs((4, 64, 64, 320), np.float16, np.float32, seed=seed,
+                                     channels_last=1, skip="nc", bias=True)
+    t = [{k: to_dev(v) for k, v in d.items()} for d in (d1, d2, d3, d4, d5)]
 
     def run():
         y1, s1 = b2.skip_rms(t[0]["input"], t[0]["skip"], t[0]["gamma"], t[0]["bias"])
@@ -32,7 +36,9 @@ def _work(seed):
                                groups=32, activation=1, channels_last=1, want_sum=True)
         y4, _ = b2.skip_group(t[3]["x"], t[3]["skip"], t[3]["gamma"], t[3]["beta"], None,
                               groups=32, activation=0, channels_last=0)
-        return [y1, s1, y2, y3, s3, y4]
+        y5, s5 = b2.skip_group(t[4]["x"], t[4]["skip"], t[4]["gamma"], t[4]["beta"], t[4]["bias"],
+                               groups=32, activation=1, channels_last=1, want_sum=True)
+        return [y1, s1, y2, y3, s3, y4, y5, s5]
     return run
 
 
