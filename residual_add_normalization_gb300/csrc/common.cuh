@@ -269,6 +269,18 @@ __device__ __forceinline__ float ld_cluster_f32(const float* local, unsigned ran
   return v;
 }
 
+// Load a float4 that CTA `rank` of this cluster holds at the same (16-byte
+// aligned) shared address as `local` does here.
+__device__ __forceinline__ float4 ld_cluster_f32x4(const float4* local, unsigned rank) {
+  unsigned addr = static_cast<unsigned>(__cvta_generic_to_shared(local));
+  unsigned remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote) : "memory");
+  return v;
+}
+
 // Sum of one value per CTA over the cluster, in rank order (identical in every
 // CTA).  `slot` is a shared float reserved for this call; the caller must
 // cluster_sync() once more before any CTA of the cluster exits.

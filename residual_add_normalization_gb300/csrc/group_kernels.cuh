@@ -5,28 +5,41 @@
 // S = round_T((X + skip) + bias); Y = round_T(act((S - mean) * rstd * gamma[c] + beta[c]))
 // with mean / population variance per (batch item n, group g) over the C/groups
 // channels of g and every spatial position (com.microsoft.SkipGroupNorm README,
-// Description).  Three routes:
+// Description).  Five routes:
 //
 //   1. NCHW resident.  A group instance (n, g) is one contiguous run of
 //      cpg * H * W elements.  One CTA -- or a cluster of up to 16 CTAs for
 //      long runs -- stages its share of S in shared memory: one HBM read,
-//      statistics from shifted sums taken while loading, one write.
-//      Cluster partials are exchanged through distributed shared memory.
+//      statistics from sums taken while loading, one write.  Cluster pieces
+//      are exchanged through distributed shared memory.
 //   2. NHWC cooperative.  A group's elements are strided through the tensor
 //      (cpg channels of every pixel), so statistics need every CTA that holds
 //      a piece of the batch item.  One cooperative grid: each CTA holds a
-//      slab of whole pixels in registers, takes its slab's per-group shifted
-//      sums, publishes them, meets the other CTAs at one bounded grid
-//      barrier, adds its batch item's partials and normalizes what it holds.
+//      slab of whole pixels in registers, takes its slab's per-group pieces,
+//      publishes them, meets the other CTAs at one bounded grid barrier,
+//      merges its batch item's pieces and normalizes what it holds.
 //   3. Two-phase, any shape or layout.  Kernel A forms S over fixed chunks of
-//      each group instance and writes per-chunk moments; kernel B merges them
+//      each group instance and writes per-chunk pieces; kernel B merges them
 //      and re-forms S from the inputs to normalize (the re-read is an L2 hit
 //      for anything that fits in L2).
+//   4. NHWC through L2, two kernels: per-CTA pieces over pixel ranges, merged
+//      by the last CTA of each batch item; then an apply kernel that re-forms
+//      S from inputs still in L2.
+//   5. Route 4's two passes in one cooperative grid with one grid barrier.
 //
-// Every route carries the group mean as K + d: K an exact data value of the
-// group (its first residual sum), d the mean of S - K.  S - K is exact for
-// data near the mean, so (S - K) - d stays accurate in binary32 even when
-// |mean| is large against the group's spread.
+// Statistics.  Every piece of a group instance that one CTA (or one cluster
+// rank, or one chunk) sees is summarised as (n, R, mu, m2): n elements, a
+// reference R near them (the mean of four of the piece's residual sums; the
+// chunk's first residual sum in route 3, whose threads sum twice from
+// registers anyway),
+// mu = mean - R and m2 = the sum of squared deviations from the mean.  The
+// sums of S - R and (S - R)^2 are taken while loading; if R turns out to be
+// far from the piece's mean against its spread (an outlier among the four
+// samples), the piece is summed again around R + mu from what the CTA holds
+// (shared memory, registers, or L2).  Pieces then merge around a common centre
+// Kc near the group mean, and every route carries the mean as Kc + d, so that
+// (S - Kc) - d stays accurate in binary32 even when |mean| is large against
+// the group's spread.
 #pragma once
 
 #include <cstring>
@@ -35,6 +48,27 @@
 #include "launch.h"
 
 namespace b200norm {
+
+// Division by an invariant divisor as a multiply and a shift (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994):
+// for 0 <= n < 2^31, n / d = (umulhi(n, m) + n) >> l with l = ceil(log2 d) and
+// m = floor(2^32 * (2^l - d) / d) + 1.
+struct FastDiv {
+  unsigned m, l;
+};
+
+inline FastDiv make_fastdiv(unsigned d) {
+  unsigned l = 0;
+  while ((1ull << l) < d) ++l;
+  FastDiv f;
+  f.m = static_cast<unsigned>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+  f.l = l;
+  return f;
+}
+
+__device__ __forceinline__ unsigned fdiv(unsigned n, FastDiv f) {
+  return (__umulhi(n, f.m) + n) >> f.l;
+}
 
 template <typename T, typename M>
 struct SgnArgs {
@@ -47,6 +81,7 @@ struct SgnArgs {
   T* __restrict__ s;            // may be null
   int64_t N;
   int C, HW, cpg, groups;
+  FastDiv cpg_div;              // division by cpg (channel -> group)
   int bcast;                    // skip holds one value per (n, c)
   int act;                      // 1: SiLU after the affine transform
   float eps;
@@ -105,34 +140,128 @@ __device__ __forceinline__ float sgn_out(float s, float K, float d, float rstd, 
   return z;
 }
 
-// Shift K of group instance (n, g): its residual sum at (channel g*cpg, pixel 0).
+// Residual sum at (batch item n, channel c, pixel p), as binary32.
 template <typename T, typename M>
-__device__ __forceinline__ float sgn_shift(const SgnArgs<T, M>& a, int64_t n, int g, bool cl) {
-  const int c = g * a.cpg;
-  const int64_t off = cl ? n * a.HW * a.C + c : (n * a.C + c) * static_cast<int64_t>(a.HW);
+__device__ __forceinline__ float sgn_at(const SgnArgs<T, M>& a, int64_t n, int c, int64_t p,
+                                        bool cl) {
+  const int64_t off = cl ? (n * a.HW + p) * a.C + c : (n * a.C + c) * a.HW + p;
   const float sk = a.bcast ? to_f32(a.skip[n * a.C + c]) : to_f32(a.skip[off]);
   return to_f32(sgn_sum<T>(to_f32(a.x[off]), sk, a.bias, c));
 }
 
-// Division by an invariant divisor as a multiply and a shift (Granlund and
-// Montgomery, "Division by invariant integers using multiplication", 1994):
-// for 0 <= n < 2^31, n / d = (umulhi(n, m) + n) >> l with l = ceil(log2 d) and
-// m = floor(2^32 * (2^l - d) / d) + 1.
-struct FastDiv {
-  unsigned m, l;
-};
+// ---------------------------------------------------------------------------
+// Group statistics from pieces
+// ---------------------------------------------------------------------------
+// A piece is a float4 (n, R, mu, m2): n elements, reference R, mu = mean - R,
+// m2 = sum of squared deviations from the mean.
+//
+// The one-pass variance s2/n - mu^2 (s1, s2 the sums of S - R and its square)
+// carries a relative error of about eps * (1 + mu^2 / var); a piece with
+// mu^2 > kIllCond * var is summed again around R + mu, so the variance keeps
+// a relative error within ~16 binary32 accumulation errors.
+constexpr float kIllCond = 15.0f;
 
-inline FastDiv make_fastdiv(unsigned d) {
-  unsigned l = 0;
-  while ((1ull << l) < d) ++l;
-  FastDiv f;
-  f.m = static_cast<unsigned>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
-  f.l = l;
-  return f;
+// Reference of a piece: the mean of four of its residual sums (each scaled
+// first, so the sum cannot overflow).  Data drawn from one distribution puts
+// it within about half a standard deviation of the piece's mean.
+__device__ __forceinline__ float ref4(float s0, float s1, float s2, float s3) {
+  return (0.25f * s0 + 0.25f * s1) + (0.25f * s2 + 0.25f * s3);
 }
 
-__device__ __forceinline__ unsigned fdiv(unsigned n, FastDiv f) {
-  return (__umulhi(n, f.m) + n) >> f.l;
+// (Counts are whole numbers, so 1 / n from the hardware reciprocal is within
+// an ulp; the statistics need nothing closer.)
+__device__ __forceinline__ float4 piece_from_sums(float n, float R, float s1, float s2) {
+  if (n == 0.0f) return make_float4(0.0f, R, 0.0f, 0.0f);
+  const float mu = s1 * rcp_approx(n);
+  return make_float4(n, R, mu, fmaxf(fmaf(-s1, mu, s2), 0.0f));
+}
+
+// Is the piece's one-pass variance too close to cancellation?  (False for
+// NaN statistics: those propagate as they are.)
+__device__ __forceinline__ bool piece_ill(float4 p) {
+  return p.z * p.z * p.x > kIllCond * p.w;
+}
+
+// Pieces merged around a centre Kc: o = (R - Kc) + mu,
+// N = sum n, s1 = sum n o, s2 = sum (m2 + n o^2); then d = s1 / N and
+// var = (s2 - s1 d) / N.  With Kc within a few standard deviations of the
+// mean (the first piece's mean, checked by merge_ill), nothing cancels.
+struct MergeAcc {
+  float n, s1, s2;
+};
+
+__device__ __forceinline__ void merge_add(MergeAcc& m, float4 p, float Kc) {
+  const float o = (p.y - Kc) + p.z;
+  const float no = p.x * o;
+  m.n += p.x;
+  m.s1 += no;
+  m.s2 += fmaf(no, o, p.w);
+}
+
+__device__ __forceinline__ void merge_add(MergeAcc& m, MergeAcc b) {
+  m.n += b.n;
+  m.s1 += b.s1;
+  m.s2 += b.s2;
+}
+
+// An accumulation around Kq, given as (Kq, n, s1, s2), moved to the centre
+// Kc and added: with dl = Kq - Kc, s1 + n dl and s2 + dl (2 s1 + n dl)
+// (exact algebra; nothing cancels while Kq is within the spread of the data
+// it summarises).
+__device__ __forceinline__ void merge_add_moved(MergeAcc& m, float4 q, float Kc) {
+  const float dl = q.x - Kc;
+  m.n += q.y;
+  m.s1 += fmaf(q.y, dl, q.z);
+  m.s2 += fmaf(dl, fmaf(q.y, dl, 2.0f * q.z), q.w);
+}
+
+// Group statistics: mean = K + d, population variance var.
+struct GStats {
+  float K, d, var;
+};
+
+__device__ __forceinline__ GStats merge_finish(MergeAcc m, float Kc) {
+  const float r = rcp_approx(m.n);
+  const float d = m.s1 * r;
+  return GStats{Kc, d, fmaxf(fmaf(-m.s1, d, m.s2), 0.0f) * r};
+}
+
+__device__ __forceinline__ bool merge_ill(GStats s) { return s.d * s.d > kIllCond * s.var; }
+
+
+// Statistics of a single piece.
+__device__ __forceinline__ GStats piece_stats(float4 p) {
+  return GStats{p.y, p.z, p.w * rcp_approx(p.x)};
+}
+
+__device__ __forceinline__ float piece_mean(float4 p) { return p.y + p.z; }
+
+// Group g's statistics from B pieces in global memory (piece b at
+// part[b * stride + g]), merged afresh: the rare path of the chunked merges,
+// kept out of line so that it costs the common path no registers.
+static __device__ __noinline__ GStats merge_pieces_global(const float4* part, int64_t stride, int g,
+                                                          int B);
+
+// B pieces get(0..B-1), merged in that order around the first piece's mean;
+// merged again around the new mean while that is far from the result (at most
+// twice more).
+template <class Get>
+__device__ __forceinline__ GStats merge_pieces(int B, Get get) {
+  float Kc = piece_mean(get(0));
+  GStats s{};
+  for (int round = 0; round < 3; ++round) {
+    MergeAcc m{0.0f, 0.0f, 0.0f};
+    for (int b = 0; b < B; ++b) merge_add(m, get(b), Kc);
+    s = merge_finish(m, Kc);
+    if (!merge_ill(s)) break;
+    Kc = Kc + s.d;
+  }
+  return s;
+}
+
+static __device__ __noinline__ GStats merge_pieces_global(const float4* part, int64_t stride, int g,
+                                                          int B) {
+  return merge_pieces(B, [&](int b) { return __ldcg(part + static_cast<int64_t>(b) * stride + g); });
 }
 
 // ---------------------------------------------------------------------------
@@ -143,8 +272,10 @@ __device__ __forceinline__ unsigned fdiv(unsigned n, FastDiv f) {
 // (n*C + g*cpg) * H*W.  CTA rank r of the instance's cluster takes vectors
 // [r * span, (r + 1) * span) of it: it loads X (+ skip), forms S, keeps S in
 // shared memory (span vectors of dynamic shared memory) and accumulates the
-// sums of S - K and (S - K)^2 on the way (K the instance's first residual sum,
-// so the shifted sums do not cancel); cluster partial sums meet through DSMEM.
+// sums of S - R and (S - R)^2 on the way (R the mean of four residual sums of
+// its range); its piece (n, R, mu, m2) is summed again from shared memory
+// when R was far from the range's mean.  A cluster's pieces meet through
+// DSMEM and every CTA merges them in rank order.
 // VE > 1 needs H*W % VE == 0 so that a vector never straddles two channels;
 // vpc = H*W / VE vectors per channel.
 #ifndef B200NORM_NCHW_UNROLL
@@ -168,7 +299,7 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
   extern __shared__ float4 smem4[];
   P* sb = reinterpret_cast<P*>(smem4);
   __shared__ float2 red2[33];
-  __shared__ float slot_sum, slot_m2;
+  __shared__ float4 slot_piece;  // this CTA's piece, read by the cluster's CTAs
   const unsigned csize = cluster_size();
   const unsigned rank = csize > 1 ? cluster_rank() : 0u;
   const int64_t inst = blockIdx.x / csize;
@@ -180,8 +311,21 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
   const int64_t base = (n * a.C + static_cast<int64_t>(g) * a.cpg) * a.HW + static_cast<int64_t>(v0) * VE;
   const int cbase = g * a.cpg;
 
-  const float K = sgn_shift(a, n, g, false);
+  // reference R: four residual sums spread over this CTA's range; threads
+  // that hold vectors take it right behind their first loads
+  auto range_ref = [&]() {
+    const int len = cnt * VE;
+    float smp[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = v0 * VE + q * (len / 4);  // element of the instance
+      smp[q] = sgn_at(a, n, cbase + j / a.HW, j % a.HW, false);
+    }
+    return ref4(smp[0], smp[1], smp[2], smp[3]);
+  };
   float sum = 0.0f, sq = 0.0f;
+  float R = 0.0f;
+  if (static_cast<int>(threadIdx.x) >= cnt && cnt > 0) R = range_ref();
   for (int i0 = threadIdx.x; i0 < cnt; i0 += kNchwThreads * kNchwUnroll) {
     P xv[kNchwUnroll], kv[kNchwUnroll];
 #pragma unroll
@@ -192,6 +336,7 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
         if (!a.bcast) kv[u] = ld_stream<T, VE>(a.skip + base + static_cast<int64_t>(i) * VE);
       }
     }
+    if (i0 == static_cast<int>(threadIdx.x)) R = range_ref();
 #pragma unroll
     for (int u = 0; u < kNchwUnroll; ++u) {
       const int i = i0 + u * kNchwThreads;
@@ -203,7 +348,7 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
         for (int e = 0; e < VE; ++e) {
           const float sk = a.bcast ? skb : to_f32(kv[u].v[e]);
           sv.v[e] = sgn_sum<T>(to_f32(xv[u].v[e]), sk, a.bias, c);
-          const float d = to_f32(sv.v[e]) - K;
+          const float d = to_f32(sv.v[e]) - R;
           sum += d;
           sq = fmaf(d, d, sq);
         }
@@ -212,14 +357,38 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
       }
     }
   }
-  // one pass of shifted sums: mean = K + dmean, var = E[(S-K)^2] - dmean^2
-  // (K is a value of the group, so |dmean| is of the order of its spread)
+  // this CTA's piece; summed again from shared memory around R + mu when R
+  // was far from the piece's mean (every thread holds the same sums, so the
+  // branch is uniform)
+  const float n_cta = static_cast<float>(max(cnt, 0) * VE);
   float2 t2 = cta_sum2(make_float2(sum, sq), red2);
-  if (csize > 1) t2 = cluster_sum2(t2, &slot_sum, &slot_m2, csize);
-  const float tot = t2.x, tsq = t2.y;
-  const float dmean = tot / static_cast<float>(L);
-  const float var = fmaxf(tsq / static_cast<float>(L) - dmean * dmean, 0.0f);
-  const float rstd = 1.0f / sqrtf(var + a.eps);
+  float4 piece = piece_from_sums(n_cta, R, t2.x, t2.y);
+  if (piece_ill(piece)) {
+    const float R2 = R + piece.z;
+    float s1 = 0.0f, s2 = 0.0f;
+    for (int i = threadIdx.x; i < cnt; i += kNchwThreads) {
+      const P sv = sb[i];
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        const float d = to_f32(sv.v[e]) - R2;
+        s1 += d;
+        s2 = fmaf(d, d, s2);
+      }
+    }
+    t2 = cta_sum2(make_float2(s1, s2), red2);
+    piece = piece_from_sums(n_cta, R2, t2.x, t2.y);
+  }
+  GStats st;
+  if (csize > 1) {
+    // the cluster's pieces, merged in rank order by every CTA (same bits)
+    if (threadIdx.x == 0) slot_piece = piece;
+    cluster_sync();
+    st = merge_pieces(static_cast<int>(csize),
+                      [&](int r) { return ld_cluster_f32x4(&slot_piece, static_cast<unsigned>(r)); });
+  } else {
+    st = piece_stats(piece);
+  }
+  const float rstd = 1.0f / sqrtf(st.var + a.eps);
   for (int i = threadIdx.x; i < cnt; i += kNchwThreads) {
     const int c = cbase + static_cast<int>(fdiv(static_cast<unsigned>(v0 + i), vpc));
     const float ga = to_f32(a.gamma[c]), be = to_f32(a.beta[c]);
@@ -227,10 +396,10 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
     P out;
 #pragma unroll
     for (int e = 0; e < VE; ++e)
-      out.v[e] = from_f32<T>(sgn_out(to_f32(sv.v[e]), K, dmean, rstd, ga, be, a.act));
+      out.v[e] = from_f32<T>(sgn_out(to_f32(sv.v[e]), st.K, st.d, rstd, ga, be, a.act));
     st_stream<T, VE>(a.y + base + static_cast<int64_t>(i) * VE, out);
   }
-  if (csize > 1) cluster_sync();  // peers may still read slot_m2
+  if (csize > 1) cluster_sync();  // peers may still read slot_piece
 }
 
 // ---------------------------------------------------------------------------
@@ -239,18 +408,41 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
 // blockDim.x = CV * PL with CV = C / VE vectors per pixel: thread t covers the
 // VE channels (t % CV) * VE .. +VE of pixels p0 + t / CV + k * PL, k < NV.
 // CTA b handles batch item b / B, pixels [(b % B) * ppc, +ppc).
-// Every CTA takes, per group, the count and the sums of S - K[g] and
-// (S - K[g])^2 over the S it holds (K[g] the group's first residual sum, the
-// same in every CTA, so the shifted sums do not cancel): per thread, per
-// pixel lane and channel, then per group.  It stores S between its arrival at
-// the grid barrier and its wait.  After the barrier each CTA adds its batch
-// item's partials in a fixed order, mean = K + d,
-// var = sum((S - K)^2) / n - d^2, and stores Y.
+// Every CTA takes, per group, the piece (count, R, mu, m2) of the S it holds:
+// sums of S - R[g] and (S - R[g])^2 per thread, pixel lane and channel, then
+// per group (R[g] the mean of four residual sums of the CTA's pixels in group
+// g); groups whose R was far from their mean are summed again from the
+// registers.  It stores S between its arrival at the grid barrier and its
+// wait.  After the barrier each CTA merges its batch item's B pieces per
+// group in a fixed order (chunks of pieces, then the chunks), and stores Y.
 // Dynamic shared memory (floats), layout given by k_offset:
-//   sums:    acc[2][PL*C] | col[2][C]
-//   merge:   chunk sums[nchunk*groups*3] | mean offset d[groups] | rstd[groups]
-//   tail at k_offset, kept throughout: K[groups] | gamma[C] | beta[C]
+//   pieces:  acc[2][PL*C] | col[2][C]
+//   merge:   chunk pieces[nchunk*groups] (float4) | centre K[groups] |
+//            offset d[groups] | rstd[groups]
+//   tail at k_offset, kept throughout: R[groups] | second-round R[groups]
+//            (padded to 16 bytes) | gamma[C] | beta[C]
 constexpr int kCoopMergeChunk = 8;
+
+// Floats of route 2's shared-memory tail before gamma (16-byte aligned).
+__host__ __device__ constexpr int coop_tail_floats(int groups) { return (2 * groups + 3) & ~3; }
+
+// Element q of the four residual sums that give group g's reference over
+// pixels [p0, p1) of batch item n (NHWC): pixel p0 + q * (p1 - p0) / 4,
+// channel g * cpg + q * cpg / 4.
+template <typename T, typename M>
+__device__ __forceinline__ float nhwc_sample(const SgnArgs<T, M>& a, int n, int g, int q, int p0,
+                                             int p1) {
+  const int p = p0 + q * ((p1 - p0) / 4);
+  const int c = g * a.cpg + (q * a.cpg) / 4;
+  return sgn_at(a, n, c, p, true);
+}
+
+// Group g's reference over pixels [p0, p1) of batch item n (NHWC).
+template <typename T, typename M>
+__device__ __forceinline__ float nhwc_ref(const SgnArgs<T, M>& a, int n, int g, int p0, int p1) {
+  return ref4(nhwc_sample(a, n, g, 0, p0, p1), nhwc_sample(a, n, g, 1, p0, p1),
+              nhwc_sample(a, n, g, 2, p0, p1), nhwc_sample(a, n, g, 3, p0, p1));
+}
 
 template <typename T, typename M, int VE, int NV>
 __global__ void __launch_bounds__(kCoopMaxThreads, 1)
@@ -259,7 +451,9 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
   pdl_trigger();
   extern __shared__ float4 smem4[];
   float* smem = reinterpret_cast<float*>(smem4);
-  float* s_K = smem + k_offset;
+  float* s_R0 = smem + k_offset;
+  float* s_R = s_R0 + a.groups;
+  __shared__ int s_again;
   const int C = a.C;
   const int CV = C / VE;
   const int PL = blockDim.x / CV;
@@ -286,17 +480,18 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
   if (a.bcast) skb = ld_reuse<T, VE>(a.skip + static_cast<int64_t>(n) * C + c0);
   if (a.bias) bv = ld_reuse<T, VE>(a.bias + c0);
   // the affine weights are needed only at the end: stage them now
-  float* s_ga = s_K + ((a.groups + 3) & ~3);  // 16-byte aligned
+  float* s_ga = s_R0 + coop_tail_floats(a.groups);  // 16-byte aligned
   float* s_be = s_ga + C;
   for (int c = threadIdx.x; c < C; c += blockDim.x) {
     s_ga[c] = to_f32(__ldg(a.gamma + c));
     s_be[c] = to_f32(__ldg(a.beta + c));
   }
-  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) s_K[gg] = sgn_shift(a, n, gg, true);
+  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) s_R0[gg] = nhwc_ref(a, n, gg, p0, p1);
+  if (threadIdx.x == 0) s_again = 0;
   __syncthreads();
   float Kl[VE];
 #pragma unroll
-  for (int e = 0; e < VE; ++e) Kl[e] = s_K[(c0 + e) / a.cpg];
+  for (int e = 0; e < VE; ++e) Kl[e] = s_R0[fdiv(c0 + e, a.cpg_div)];
   float lsum[VE], lsq[VE];
 #pragma unroll
   for (int e = 0; e < VE; ++e) lsum[e] = lsq[e] = 0.0f;
@@ -314,39 +509,68 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
       }
     }
   }
-  // --- CTA sums of S - K and (S - K)^2 per group ---------------------------
+  // --- this CTA's pieces, per group ----------------------------------------
   // acc is laid out [q][e][tp][tc] so that the stores of a warp hit distinct
-  // banks; col is [q][C]
+  // banks; col is [q][C].  A second round (from the registers, around
+  // R + mu) runs only when some group's R was far from its mean.
   float* s_acc = smem;
   float* s_col = smem + 2 * PL * C;
   const int nthr = PL * CV;
-#pragma unroll
-  for (int e = 0; e < VE; ++e) {
-    s_acc[(e * PL + tp) * CV + tc] = lsum[e];
-    s_acc[nthr * VE + (e * PL + tp) * CV + tc] = lsq[e];
-  }
-  __syncthreads();
-  for (int j = threadIdx.x; j < C; j += blockDim.x) {
-    const int e = j / CV, q0 = j % CV;
-    float t1 = 0.0f, t2 = 0.0f;
-    for (int q = 0; q < PL; ++q) {
-      t1 += s_acc[(e * PL + q) * CV + q0];
-      t2 += s_acc[nthr * VE + (e * PL + q) * CV + q0];
-    }
-    s_col[q0 * VE + e] = t1;
-    s_col[C + q0 * VE + e] = t2;
-  }
-  __syncthreads();
   const float n_cta = static_cast<float>(p1 - p0) * static_cast<float>(a.cpg);
-  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
-    float t1 = 0.0f, t2 = 0.0f;
-    for (int cc = 0; cc < a.cpg; ++cc) {
-      t1 += s_col[gg * a.cpg + cc];
-      t2 += s_col[C + gg * a.cpg + cc];
+  for (int round = 0; round < 2; ++round) {
+    if (round == 1) {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        Kl[e] = s_R[fdiv(c0 + e, a.cpg_div)];
+        lsum[e] = lsq[e] = 0.0f;
+      }
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        if (p0 + tp + k * PL < p1) {
+#pragma unroll
+          for (int e = 0; e < VE; ++e) {
+            const float d = to_f32(sv[k].v[e]) - Kl[e];
+            lsum[e] += d;
+            lsq[e] = fmaf(d, d, lsq[e]);
+          }
+        }
+      }
     }
-    a.part[static_cast<int64_t>(blockIdx.x) * a.groups + gg] = make_float4(n_cta, t1, t2, 0.0f);
+#pragma unroll
+    for (int e = 0; e < VE; ++e) {
+      s_acc[(e * PL + tp) * CV + tc] = lsum[e];
+      s_acc[nthr * VE + (e * PL + tp) * CV + tc] = lsq[e];
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < C; j += blockDim.x) {
+      const int e = j / CV, q0 = j % CV;
+      float t1 = 0.0f, t2 = 0.0f;
+      for (int q = 0; q < PL; ++q) {
+        t1 += s_acc[(e * PL + q) * CV + q0];
+        t2 += s_acc[nthr * VE + (e * PL + q) * CV + q0];
+      }
+      s_col[q0 * VE + e] = t1;
+      s_col[C + q0 * VE + e] = t2;
+    }
+    __syncthreads();
+    for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
+      float t1 = 0.0f, t2 = 0.0f;
+      for (int cc = 0; cc < a.cpg; ++cc) {
+        t1 += s_col[gg * a.cpg + cc];
+        t2 += s_col[C + gg * a.cpg + cc];
+      }
+      const float R = round == 0 ? s_R0[gg] : s_R[gg];
+      const float4 piece = piece_from_sums(n_cta, R, t1, t2);
+      a.part[static_cast<int64_t>(blockIdx.x) * a.groups + gg] = piece;
+      if (round == 0) {
+        s_R[gg] = R + piece.z;
+        if (piece_ill(piece)) s_again = 1;
+      }
+    }
+    __syncthreads();
+    if (!s_again) break;
   }
-  // the arrival's release (after a CTA barrier) publishes these partials; S,
+  // the arrival's release (after a CTA barrier) publishes these pieces; S,
   // which no other CTA reads, is stored while the other CTAs arrive
   grid_arrive(a.ctl);
   if (a.s) {
@@ -362,14 +586,16 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
     return;
   }
 
-  // --- add the batch item's B partials per group (every CTA shifts by the
-  // same K, so plain sums in a fixed order) -----------------------------------
-  // chunks of kCoopMergeChunk partials: all loads of a chunk are issued
-  // before they are added, then the chunk sums are added per group
+  // --- merge the batch item's B pieces per group in a fixed order (every CTA
+  // of the item gets the same bits): chunks of kCoopMergeChunk pieces, each
+  // summed around its first piece's mean Kq (all loads of a chunk issued
+  // before they are added) and kept as (Kq, n, s1, s2); then the chunks,
+  // moved to the first chunk's Kq ---------------------------------------------
   const int nchunk = (B + kCoopMergeChunk - 1) / kCoopMergeChunk;
-  float* s_cm = smem;                                  // nchunk * groups * 3
-  float* s_gmean = smem + nchunk * a.groups * 3;
-  float* s_grstd = s_gmean + a.groups;
+  float4* s_cp = reinterpret_cast<float4*>(smem);      // nchunk * groups
+  float* s_gK = smem + nchunk * a.groups * 4;
+  float* s_gd = s_gK + a.groups;
+  float* s_grstd = s_gd + a.groups;
   const float4* src = a.part + static_cast<int64_t>(n) * B * a.groups;
   for (int idx = threadIdx.x; idx < nchunk * a.groups; idx += blockDim.x) {
     const int gg = idx % a.groups, q = idx / a.groups;
@@ -378,38 +604,34 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
 #pragma unroll
     for (int j = 0; j < kCoopMergeChunk; ++j)
       if (b0 + j < B) u[j] = __ldcg(src + static_cast<int64_t>(b0 + j) * a.groups + gg);
-    float cn = 0.0f, c1 = 0.0f, c2 = 0.0f;
+    const float Kq = piece_mean(u[0]);
+    MergeAcc m{0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int j = 0; j < kCoopMergeChunk; ++j)
-      if (b0 + j < B) {
-        cn += u[j].x;
-        c1 += u[j].y;
-        c2 += u[j].z;
-      }
-    s_cm[idx * 3] = cn;
-    s_cm[idx * 3 + 1] = c1;
-    s_cm[idx * 3 + 2] = c2;
+      if (b0 + j < B) merge_add(m, u[j], Kq);
+    s_cp[idx] = make_float4(Kq, m.n, m.s1, m.s2);
   }
   __syncthreads();
   for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
-    float cn = 0.0f, c1 = 0.0f, c2 = 0.0f;
-    for (int q = 0; q < nchunk; ++q) {
-      const int idx = q * a.groups + gg;
-      cn += s_cm[idx * 3];
-      c1 += s_cm[idx * 3 + 1];
-      c2 += s_cm[idx * 3 + 2];
-    }
-    const float d = c1 / cn;
-    s_gmean[gg] = d;
-    s_grstd[gg] = 1.0f / sqrtf(fmaxf(c2 / cn - d * d, 0.0f) + a.eps);
+    const float Kc = s_cp[gg].x;
+    MergeAcc m{0.0f, 0.0f, 0.0f};
+    for (int q = 0; q < nchunk; ++q) merge_add_moved(m, s_cp[q * a.groups + gg], Kc);
+    GStats st = merge_finish(m, Kc);
+    if (merge_ill(st))  // pathological spread of the pieces: merge them all afresh
+      st = merge_pieces_global(src, a.groups, gg, B);
+    s_gK[gg] = st.K;
+    s_gd[gg] = st.d;
+    s_grstd[gg] = 1.0f / sqrtf(st.var + a.eps);
   }
   __syncthreads();
   // --- normalize what this thread holds; store Y ---------------------------
-  float mu[VE], rs[VE];
+  float Kg[VE], mu[VE], rs[VE];
 #pragma unroll
   for (int e = 0; e < VE; ++e) {
-    mu[e] = s_gmean[(c0 + e) / a.cpg];
-    rs[e] = s_grstd[(c0 + e) / a.cpg];
+    const unsigned ge = fdiv(c0 + e, a.cpg_div);
+    Kg[e] = s_gK[ge];
+    mu[e] = s_gd[ge];
+    rs[e] = s_grstd[ge];
   }
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
@@ -422,7 +644,7 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
       Pack<T, VE> out;
 #pragma unroll
       for (int e = 0; e < VE; ++e)
-        out.v[e] = from_f32<T>(sgn_out(to_f32(sv[k].v[e]), Kl[e], mu[e], rs[e], ga[e], be[e],
+        out.v[e] = from_f32<T>(sgn_out(to_f32(sv[k].v[e]), Kg[e], mu[e], rs[e], ga[e], be[e],
                                        a.act));
       st_stream<T, VE>(a.y + off, out);
     }
@@ -463,22 +685,25 @@ constexpr int kL2MaxThreads = 512;
 constexpr int64_t kL2RouteMaxBytes = 48ll << 20;  // re-read through the 129 MB L2
 
 // Shared memory of the per-CTA statistics: per-thread sums [2][VE][PL][CV],
-// later the merge slices [3][S][groups].
+// later the merge slices' pieces [S][groups] (float4).
 template <int VE>
 __host__ __device__ constexpr int nhwc_red_floats() {
   return 2 * kL2MaxThreads * VE > 3 * 1024 ? 2 * kL2MaxThreads * VE : 3 * 1024;
 }
 
-// One CTA's statistics over pixels [p0, p1) of batch item n (routes 4 and 5):
-// K[g] into s_K, then per group the sums of S - K[g] and (S - K[g])^2 and the
-// element count, written to part[b * groups + g] as (sum, sum of squares,
-// count, 0).  X and skip are read with the default cache policy, so that the
-// second pass finds them in L2.  Every thread of the CTA calls it; it ends
-// with the partial stores issued (no barrier after them).
+// One CTA's pieces over pixels [p0, p1) of batch item n (routes 4 and 5):
+// each group's reference (the mean of four of its residual sums in the range)
+// into s_ref[g], then per group the piece (count, R, mu, m2) of its residual
+// sums, written to part[b * groups + g]; when some group's R was far from its
+// mean, the pixel range is walked again (from L2) around R + mu, kept in
+// s_ref[groups + g].  X and skip are read with the default cache policy, so that later
+// passes find them in L2.  Every thread of the CTA calls it; it ends with a
+// CTA barrier after the piece stores.
 template <typename T, typename M, int VE, bool BC, int PASSES = kL2Passes>
 __device__ __forceinline__ void nhwc_partials(const SgnArgs<T, M>& a, int n, int b, int p0,
-                                              int p1, float* s_K, float* s_red, float* s_col,
+                                              int p1, float* s_ref, float* s_red, float* s_col,
                                               float4* part) {
+  __shared__ int s_again;
   const int C = a.C;
   const int CV = C / VE;
   const int PL = blockDim.x / CV;
@@ -487,123 +712,141 @@ __device__ __forceinline__ void nhwc_partials(const SgnArgs<T, M>& a, int n, int
   const int64_t nbase = static_cast<int64_t>(n) * a.HW * C;
   const int c0 = tc * VE;
   const bool active = tp < PL;
+  float* s_R0 = s_ref;
+  float* s_R = s_ref + a.groups;
 
-  for (int g = threadIdx.x; g < a.groups; g += blockDim.x) s_K[g] = sgn_shift(a, n, g, true);
+  for (int g = threadIdx.x; g < a.groups; g += blockDim.x) s_R0[g] = nhwc_ref(a, n, g, p0, p1);
+  if (threadIdx.x == 0) s_again = 0;
   Pack<T, VE> skb, bv;
   if (active) {
     if constexpr (BC) skb = ld_reuse<T, VE>(a.skip + static_cast<int64_t>(n) * C + c0);
     if (a.bias) bv = ld_reuse<T, VE>(a.bias + c0);
   }
   __syncthreads();
-  float s1[VE], s2[VE];
+  float Kl[VE];
 #pragma unroll
-  for (int e = 0; e < VE; ++e) s1[e] = s2[e] = 0.0f;
-  if (active) {
-    float Kl[VE];
+  for (int e = 0; e < VE; ++e) Kl[e] = s_R0[fdiv(c0 + e, a.cpg_div)];
+  const int nthr = PL * CV;
+  const float cnt = static_cast<float>(p1 - p0) * static_cast<float>(a.cpg);
+  for (int round = 0; round < 2; ++round) {
+    if (round == 1) {
 #pragma unroll
-    for (int e = 0; e < VE; ++e) Kl[e] = s_K[(c0 + e) / a.cpg];
-    for (int q = p0 + tp; q < p1; q += PASSES * PL) {
-      Pack<T, VE> xv[PASSES], kv[BC ? 1 : PASSES];
+      for (int e = 0; e < VE; ++e) Kl[e] = s_R[fdiv(c0 + e, a.cpg_div)];
+    }
+    float s1[VE], s2[VE];
 #pragma unroll
-      for (int k = 0; k < PASSES; ++k) {
-        const int p = q + k * PL;
-        if (p < p1) {
-          const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
-          xv[k] = ld_reuse<T, VE>(a.x + off);
-          if constexpr (!BC) kv[k] = ld_reuse<T, VE>(a.skip + off);
+    for (int e = 0; e < VE; ++e) s1[e] = s2[e] = 0.0f;
+    if (active) {
+      for (int q = p0 + tp; q < p1; q += PASSES * PL) {
+        Pack<T, VE> xv[PASSES], kv[BC ? 1 : PASSES];
+#pragma unroll
+        for (int k = 0; k < PASSES; ++k) {
+          const int p = q + k * PL;
+          if (p < p1) {
+            const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+            xv[k] = ld_reuse<T, VE>(a.x + off);
+            if constexpr (!BC) kv[k] = ld_reuse<T, VE>(a.skip + off);
+          }
         }
-      }
 #pragma unroll
-      for (int k = 0; k < PASSES; ++k) {
-        if (q + k * PL < p1) {
+        for (int k = 0; k < PASSES; ++k) {
+          if (q + k * PL < p1) {
 #pragma unroll
-          for (int e = 0; e < VE; ++e) {
-            const float sk = BC ? to_f32(skb.v[e]) : to_f32(kv[BC ? 0 : k].v[e]);
-            const float d = to_f32(sgn_sum_b<T>(to_f32(xv[k].v[e]), sk, to_f32(bv.v[e]),
-                                                a.bias != nullptr)) -
-                            Kl[e];
-            s1[e] += d;
-            s2[e] = fmaf(d, d, s2[e]);
+            for (int e = 0; e < VE; ++e) {
+              const float sk = BC ? to_f32(skb.v[e]) : to_f32(kv[BC ? 0 : k].v[e]);
+              const float d = to_f32(sgn_sum_b<T>(to_f32(xv[k].v[e]), sk, to_f32(bv.v[e]),
+                                                  a.bias != nullptr)) -
+                              Kl[e];
+              s1[e] += d;
+              s2[e] = fmaf(d, d, s2[e]);
+            }
           }
         }
       }
     }
-  }
-  // per channel (over the pixel lanes), then per group
-  const int nthr = PL * CV;
-  if (active) {
+    // per channel (over the pixel lanes), then per group
+    if (active) {
 #pragma unroll
-    for (int e = 0; e < VE; ++e) {
-      s_red[(e * PL + tp) * CV + tc] = s1[e];
-      s_red[nthr * VE + (e * PL + tp) * CV + tc] = s2[e];
+      for (int e = 0; e < VE; ++e) {
+        s_red[(e * PL + tp) * CV + tc] = s1[e];
+        s_red[nthr * VE + (e * PL + tp) * CV + tc] = s2[e];
+      }
     }
-  }
-  __syncthreads();
-  for (int j = threadIdx.x; j < C; j += blockDim.x) {
-    const int e = j / CV, q0 = j % CV;
-    float t1 = 0.0f, t2 = 0.0f;
-    for (int q = 0; q < PL; ++q) {
-      t1 += s_red[(e * PL + q) * CV + q0];
-      t2 += s_red[nthr * VE + (e * PL + q) * CV + q0];
+    __syncthreads();
+    for (int j = threadIdx.x; j < C; j += blockDim.x) {
+      const int e = j / CV, q0 = j % CV;
+      float t1 = 0.0f, t2 = 0.0f;
+      for (int q = 0; q < PL; ++q) {
+        t1 += s_red[(e * PL + q) * CV + q0];
+        t2 += s_red[nthr * VE + (e * PL + q) * CV + q0];
+      }
+      s_col[q0 * VE + e] = t1;
+      s_col[C + q0 * VE + e] = t2;
     }
-    s_col[q0 * VE + e] = t1;
-    s_col[C + q0 * VE + e] = t2;
-  }
-  __syncthreads();
-  const float cnt = static_cast<float>(p1 - p0) * static_cast<float>(a.cpg);
-  for (int g = threadIdx.x; g < a.groups; g += blockDim.x) {
-    float t1 = 0.0f, t2 = 0.0f;
-    for (int cc = 0; cc < a.cpg; ++cc) {
-      t1 += s_col[g * a.cpg + cc];
-      t2 += s_col[C + g * a.cpg + cc];
+    __syncthreads();
+    for (int g = threadIdx.x; g < a.groups; g += blockDim.x) {
+      float t1 = 0.0f, t2 = 0.0f;
+      for (int cc = 0; cc < a.cpg; ++cc) {
+        t1 += s_col[g * a.cpg + cc];
+        t2 += s_col[C + g * a.cpg + cc];
+      }
+      const float R = round == 0 ? s_R0[g] : s_R[g];
+      const float4 piece = piece_from_sums(cnt, R, t1, t2);
+      part[static_cast<int64_t>(b) * a.groups + g] = piece;
+      if (round == 0) {
+        s_R[g] = R + piece.z;
+        if (piece_ill(piece)) s_again = 1;
+      }
     }
-    part[static_cast<int64_t>(b) * a.groups + g] = make_float4(t1, t2, cnt, 0.0f);
+    __syncthreads();
+    if (!s_again) break;
   }
 }
 
-// Adds a batch item's B partials per group in a fixed order: slice j of group
-// g adds partials j, j + S, j + 2S, ... (S slices per group, the block's
-// threads spread over groups x slices), then the slices are added in order,
-// so every CTA that merges gets the same bits.  Leaves (d, rstd) of group g in
-// s_out[g] and s_out[groups + g]; ends with a barrier.
+// Merges a batch item's B pieces per group in a fixed order: slice j of group
+// g sums pieces j, j + S, j + 2S, ... (S slices per group, the block's
+// threads spread over groups x slices) around the mean Kq of its first piece,
+// kept as (Kq, n, s1, s2); then the slices are moved to the first slice's Kq
+// and added in order, so every CTA that merges gets the same bits.  Leaves the
+// centre K, the offset d of the mean and rstd of group g in s_out[g],
+// s_out[groups + g] and s_out[2 * groups + g]; ends with a barrier.  s_m holds
+// S * groups float4.
 template <typename T, typename M>
 __device__ __forceinline__ void nhwc_merge(const SgnArgs<T, M>& a, const float4* part, int B,
-                                           float* s_m, float* s_out) {
+                                           float4* s_m, float* s_out) {
   const int S = max(1, static_cast<int>(blockDim.x) / a.groups);
   for (int idx = threadIdx.x; idx < S * a.groups; idx += blockDim.x) {
     const int g = idx % a.groups, j = idx / a.groups;
-    float t1 = 0.0f, t2 = 0.0f, c = 0.0f;
-    // eight loads in flight per batch; slots past B add +0, which leaves every
-    // sum's bits as they would be without them
+    MergeAcc m{0.0f, 0.0f, 0.0f};
+    float Kq = 0.0f;
+    // eight loads in flight per batch; slots past B are empty pieces centred
+    // on Kq, which add +0 to every sum
     for (int q = j; q < B; q += 8 * S) {
       float4 u[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         u[i] = q + i * S < B ? __ldcg(part + static_cast<int64_t>(q + i * S) * a.groups + g)
                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (q == j) Kq = piece_mean(u[0]);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        t1 += u[i].x;
-        t2 += u[i].y;
-        c += u[i].z;
+        if (q + i * S >= B) u[i].y = Kq;
+        merge_add(m, u[i], Kq);
       }
     }
-    s_m[(0 * S + j) * a.groups + g] = t1;
-    s_m[(1 * S + j) * a.groups + g] = t2;
-    s_m[(2 * S + j) * a.groups + g] = c;
+    s_m[j * a.groups + g] = make_float4(Kq, m.n, m.s1, m.s2);
   }
   __syncthreads();
   for (int g = threadIdx.x; g < a.groups; g += blockDim.x) {
-    float t1 = 0.0f, t2 = 0.0f, c = 0.0f;
-    for (int j = 0; j < S; ++j) {
-      t1 += s_m[(0 * S + j) * a.groups + g];
-      t2 += s_m[(1 * S + j) * a.groups + g];
-      c += s_m[(2 * S + j) * a.groups + g];
-    }
-    const float d = t1 / c;
-    const float var = fmaxf(t2 / c - d * d, 0.0f);
-    s_out[g] = d;
-    s_out[a.groups + g] = 1.0f / sqrtf(var + a.eps);
+    const float Kc = s_m[g].x;
+    MergeAcc m{0.0f, 0.0f, 0.0f};
+    for (int j = 0; j < min(S, B); ++j) merge_add_moved(m, s_m[j * a.groups + g], Kc);
+    GStats st = merge_finish(m, Kc);
+    if (merge_ill(st))  // pathological spread of the pieces: merge them all afresh
+      st = merge_pieces_global(part, a.groups, g, B);
+    s_out[g] = st.K;
+    s_out[a.groups + g] = st.d;
+    s_out[2 * a.groups + g] = 1.0f / sqrtf(st.var + a.eps);
   }
   __syncthreads();
 }
@@ -613,21 +856,21 @@ __global__ void __launch_bounds__(kL2MaxThreads, 2)
 sgn_nhwc_stats(const SgnArgs<T, M> a, int B, int ppc) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float s_red[nhwc_red_floats<VE>()];
-  __shared__ float s_col[2 * 1024];  // [2][C], C <= 1024
+  __shared__ __align__(16) float s_red[nhwc_red_floats<VE>()];
+  __shared__ float s_col[3 * 1024];  // [2][C], C <= 1024; then (K, d, rstd) per group
   __shared__ unsigned s_last;
-  extern __shared__ float s_K[];  // [groups]
+  extern __shared__ float s_ref[];  // [2 * groups]
   const int n = blockIdx.x / B;
   const int b = blockIdx.x % B;
   const int p0 = b * ppc;
   const int p1 = min(p0 + ppc, a.HW);
   float4* part = a.part + static_cast<int64_t>(n) * B * a.groups;
-  nhwc_partials<T, M, VE, BC>(a, n, b, p0, p1, s_K, s_red, s_col, part);
-  // The last CTA of this batch item merges its partials.  The barrier orders
-  // every thread's partial stores before thread 0's fence, and the fence
-  // (cumulative) makes them visible GPU-wide before the count goes up; on
-  // the merging side the fence after the count orders the reads after it.
-  __syncthreads();
+  nhwc_partials<T, M, VE, BC>(a, n, b, p0, p1, s_ref, s_red, s_col, part);
+  // The last CTA of this batch item merges its pieces.  The barrier at the
+  // end of nhwc_partials orders every thread's piece stores before thread 0's
+  // fence, and the fence (cumulative) makes them visible GPU-wide before the
+  // count goes up; on the merging side the fence after the count orders the
+  // reads after it.
   float4* stats = a.part + a.N * B * a.groups;
   unsigned* counter = a.ctl->item_done + n;
   if (threadIdx.x == 0) {
@@ -637,10 +880,10 @@ sgn_nhwc_stats(const SgnArgs<T, M> a, int B, int ppc) {
   }
   __syncthreads();
   if (!s_last) return;
-  nhwc_merge(a, part, B, s_red, s_col);
+  nhwc_merge(a, part, B, reinterpret_cast<float4*>(s_red), s_col);
   for (int g = threadIdx.x; g < a.groups; g += blockDim.x)
     stats[static_cast<int64_t>(n) * a.groups + g] =
-        make_float4(s_K[g], s_col[g], s_col[a.groups + g], 0.0f);
+        make_float4(s_col[g], s_col[a.groups + g], s_col[2 * a.groups + g], 0.0f);
   if (threadIdx.x == 0) *counter = 0u;  // ready for the next call
 }
 
@@ -732,15 +975,15 @@ sgn_nhwc_apply(const SgnArgs<T, M> a, int B, int ppc) {
 // writing S and Y.  No second launch, and no last-CTA merge that the rest of
 // the grid waits for.  Needs every CTA resident at once (a cooperative
 // launch) and the inputs to stay in L2 between the passes (as route 4).
-// Dynamic shared memory: table [C] float4 | K [groups] float.
+// Dynamic shared memory: table [C] float4 | references [2 * groups] float.
 template <typename T, typename M, int VE, bool BC>
 __global__ void __launch_bounds__(kL2MaxThreads, 2)
 sgn_nhwc_coop_l2(const SgnArgs<T, M> a, int B, int ppc) {
-  __shared__ float s_red[nhwc_red_floats<VE>()];
-  __shared__ float s_col[2 * 1024];  // [2][C], C <= 1024; then (d, rstd) per group
+  __shared__ __align__(16) float s_red[nhwc_red_floats<VE>()];
+  __shared__ float s_col[3 * 1024];  // [2][C], C <= 1024; then (K, d, rstd) per group
   extern __shared__ float4 s_dyn[];
   float4* s_coef = s_dyn;
-  float* s_K = reinterpret_cast<float*>(s_dyn + a.C);
+  float* s_ref = reinterpret_cast<float*>(s_dyn + a.C);  // [2 * groups]
   const int C = a.C;
   const int CV = C / VE;
   const int PL = blockDim.x / CV;
@@ -754,7 +997,7 @@ sgn_nhwc_coop_l2(const SgnArgs<T, M> a, int B, int ppc) {
   const int c0 = tc * VE;
   float4* part = a.part + static_cast<int64_t>(n) * B * a.groups;
 
-  nhwc_partials<T, M, VE, BC, kCoopL2Passes>(a, n, b, p0, p1, s_K, s_red, s_col, part);
+  nhwc_partials<T, M, VE, BC, kCoopL2Passes>(a, n, b, p0, p1, s_ref, s_red, s_col, part);
   // the arrival's release (after a CTA barrier) publishes the partials
   grid_arrive(a.ctl);
   unsigned departure = 0u;
@@ -762,11 +1005,12 @@ sgn_nhwc_coop_l2(const SgnArgs<T, M> a, int B, int ppc) {
     grid_depart(a.ctl, departure);
     return;
   }
-  nhwc_merge(a, part, B, s_red, s_col);
+  nhwc_merge(a, part, B, reinterpret_cast<float4*>(s_red), s_col);
   for (int c = threadIdx.x; c < C; c += blockDim.x) {
     const int g = c / a.cpg;
     s_coef[(c % VE) * CV + c / VE] =
-        make_float4(s_K[g], s_col[g], s_col[a.groups + g] * to_f32(__ldg(a.gamma + c)),
+        make_float4(s_col[g], s_col[a.groups + g],
+                    s_col[2 * a.groups + g] * to_f32(__ldg(a.gamma + c)),
                     to_f32(__ldg(a.beta + c)));
   }
   __syncthreads();
@@ -850,6 +1094,11 @@ __device__ __forceinline__ void smem_merge(float* mn, float* mm, float* m2, int 
   }
 }
 
+// Kernel A: the piece (count, R, mu, m2) of one chunk of kTwoPhaseChunk
+// elements of a group instance, R the chunk's first residual sum: each
+// thread's elements are held in registers and summed twice (mean, then the
+// squared deviations from it), and the threads' moments meet in a tree of
+// Chan merges, all around R.
 template <typename T, typename M, bool CL>
 __global__ void __launch_bounds__(kTwoPhaseThreads)
 sgn_partials(const SgnArgs<T, M> a, int chunks) {
@@ -862,7 +1111,10 @@ sgn_partials(const SgnArgs<T, M> a, int chunks) {
   const int g = static_cast<int>(inst % a.groups);
   const int64_t L = static_cast<int64_t>(a.cpg) * a.HW;
   const int64_t j0 = static_cast<int64_t>(q) * kTwoPhaseChunk;
-  const float K = sgn_shift(a, n, g, CL);
+  int64_t off0;
+  int cr;
+  sgn_locate(a, n, g, j0, CL, &off0, &cr);
+  const float R = sgn_form(a, n, off0, cr);
   float v[kTwoPhaseEpt];
   int cnt = 0;
   float sum = 0.0f;
@@ -878,7 +1130,7 @@ sgn_partials(const SgnArgs<T, M> a, int chunks) {
       const float sk = a.bcast ? to_f32(a.skip[n * a.C + c]) : to_f32(__ldcs(a.skip + off));
       const T sT = sgn_sum<T>(x, sk, a.bias, c);
       if (a.s) a.s[off] = sT;
-      v[i] = to_f32(sT) - K;
+      v[i] = to_f32(sT) - R;
       sum += v[i];
       ++cnt;
     }
@@ -898,40 +1150,36 @@ sgn_partials(const SgnArgs<T, M> a, int chunks) {
   m2s[threadIdx.x] = m2;
   __syncthreads();
   smem_merge(mn, mm, m2s, blockDim.x);
-  if (threadIdx.x == 0) a.part[blockIdx.x] = make_float4(mn[0], mm[0], m2s[0], 0.0f);
+  if (threadIdx.x == 0) a.part[blockIdx.x] = make_float4(mn[0], R, mm[0], m2s[0]);
 }
 
+// Kernel B: merges the instance's chunk pieces around the first chunk's mean
+// (again around the merged mean when that was far from it), re-forms S from
+// the inputs and writes Y.
 template <typename T, typename M, bool CL>
 __global__ void __launch_bounds__(kTwoPhaseThreads)
 sgn_normalize(const SgnArgs<T, M> a, int chunks) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float mn[kTwoPhaseThreads], mm[kTwoPhaseThreads], m2s[kTwoPhaseThreads];
-  __shared__ float s_mean, s_rstd;
+  __shared__ float2 red2[33];
   const int64_t inst = blockIdx.x / chunks;
   const int q = blockIdx.x % chunks;
   const int64_t n = inst / a.groups;
   const int g = static_cast<int>(inst % a.groups);
   const int64_t L = static_cast<int64_t>(a.cpg) * a.HW;
-  // merge this instance's chunk moments: each thread folds a strided subset
-  // in order, then a tree over threads
-  Moments m{0.0f, 0.0f, 0.0f};
-  for (int i = threadIdx.x; i < chunks; i += blockDim.x) {
-    const float4 u = __ldcg(a.part + inst * chunks + i);
-    m = merge(m, Moments{u.x, u.y, u.z});
+  const float4* cp = a.part + inst * chunks;
+  float Kc = piece_mean(__ldcg(cp));
+  GStats st{};
+  for (int round = 0; round < 3; ++round) {
+    MergeAcc m{0.0f, 0.0f, 0.0f};
+    for (int i = threadIdx.x; i < chunks; i += blockDim.x) merge_add(m, __ldcg(cp + i), Kc);
+    const float2 t = cta_sum2(make_float2(m.n, m.s1), red2);
+    const float2 u = cta_sum2(make_float2(m.s2, 0.0f), red2);
+    st = merge_finish(MergeAcc{t.x, t.y, u.x}, Kc);
+    if (!merge_ill(st)) break;  // uniform: every thread holds the same totals
+    Kc = Kc + st.d;
   }
-  mn[threadIdx.x] = m.n;
-  mm[threadIdx.x] = m.mean;
-  m2s[threadIdx.x] = m.m2;
-  __syncthreads();
-  smem_merge(mn, mm, m2s, blockDim.x);
-  if (threadIdx.x == 0) {
-    s_mean = mm[0];
-    s_rstd = 1.0f / sqrtf(m2s[0] / mn[0] + a.eps);
-  }
-  __syncthreads();
-  const float dmean = s_mean, rstd = s_rstd;
-  const float K = sgn_shift(a, n, g, CL);
+  const float rstd = 1.0f / sqrtf(st.var + a.eps);
   const int64_t j0 = static_cast<int64_t>(q) * kTwoPhaseChunk;
 #pragma unroll 4
   for (int i = 0; i < kTwoPhaseEpt; ++i) {
@@ -942,7 +1190,7 @@ sgn_normalize(const SgnArgs<T, M> a, int chunks) {
       sgn_locate(a, n, g, j, CL, &off, &c);
       const float sv = sgn_form(a, n, off, c);
       a.y[off] = from_f32<T>(
-          sgn_out(sv, K, dmean, rstd, to_f32(a.gamma[c]), to_f32(a.beta[c]), a.act));
+          sgn_out(sv, st.K, st.d, rstd, to_f32(a.gamma[c]), to_f32(a.beta[c]), a.act));
     }
   }
 }
@@ -950,12 +1198,12 @@ sgn_normalize(const SgnArgs<T, M> a, int chunks) {
 // ---------------------------------------------------------------------------
 // Kernel selection and typed launch (host)
 // ---------------------------------------------------------------------------
-// Offset (in floats) of the K[groups] | gamma | beta tail of route 2's dynamic
-// shared memory: past both the sums area and the merge area.
+// Offset (in floats) of the samples | R | gamma | beta tail of route 2's
+// dynamic shared memory: past both the pieces area and the merge area.
 inline size_t coop_k_offset(int PL, int C, int B, int groups) {
   const size_t passes = 2 * (static_cast<size_t>(PL) * C + C);
   const size_t nchunk = (static_cast<size_t>(B) + kCoopMergeChunk - 1) / kCoopMergeChunk;
-  const size_t merge = nchunk * groups * 3 + 2ull * groups;
+  const size_t merge = nchunk * groups * 4 + 3ull * groups;
   const size_t off = passes > merge ? passes : merge;
   return (off + 3) & ~static_cast<size_t>(3);  // 16-byte aligned tail
 }
@@ -977,10 +1225,16 @@ inline void* pick_coop(int ve, int nv) {
     }
     return nullptr;
   }
+  // 3, 5 and 6 pixels per thread too: the tightest count that holds a slab
+  // keeps the fewest registers live (the NHWC fp16 workload's 54-pixel slabs
+  // over 12 pixel lanes take 5; 8 spills)
   switch (nv) {
     case 1: return coop_fn<T, M, V16, 1>();
     case 2: return coop_fn<T, M, V16, 2>();
+    case 3: return coop_fn<T, M, V16, 3>();
     case 4: return coop_fn<T, M, V16, 4>();
+    case 5: return coop_fn<T, M, V16, 5>();
+    case 6: return coop_fn<T, M, V16, 6>();
     case 8: return coop_fn<T, M, V16, 8>();
   }
   return nullptr;
@@ -1039,6 +1293,7 @@ inline cudaError_t launch_group_typed(const SkipGroupCall& c, const GroupPlan& p
   a.HW = static_cast<int>(c.H * c.W);
   a.cpg = static_cast<int>(c.C / c.groups);
   a.groups = c.groups;
+  a.cpg_div = make_fastdiv(static_cast<unsigned>(a.cpg));
   a.bcast = c.bcast ? 1 : 0;
   a.act = c.activation;
   a.eps = c.eps;
@@ -1103,7 +1358,7 @@ inline cudaError_t launch_group_typed(const SkipGroupCall& c, const GroupPlan& p
     void* args[] = {&a, &B, &ppc};
     cfg.attrs = attr;
     cfg.numAttrs = add_pdl_attr(attr, 0);
-    cfg.dynamicSmemBytes = static_cast<size_t>(c.groups) * sizeof(float);
+    cfg.dynamicSmemBytes = static_cast<size_t>(2 * c.groups) * sizeof(float);
     cudaError_t e = cudaLaunchKernelExC(&cfg, stats, args);
     if (e != cudaSuccess) return e;
     cfg.dynamicSmemBytes = p.smem;

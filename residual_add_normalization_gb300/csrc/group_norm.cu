@@ -124,9 +124,10 @@ static bool allow_smem(void* fn, size_t smem, int dev) {
 }
 
 // Dynamic shared memory of route 2: the phase area up to coop_k_offset, then
-// K[groups] (padded to 16 bytes), gamma[C] and beta[C].
+// R[groups] and the second-round R[groups] (padded to 16 bytes), gamma[C]
+// and beta[C].
 static size_t coop_smem_bytes(int PL, int C, int B, int groups) {
-  return (coop_k_offset(PL, C, B, groups) + ((groups + 3) & ~3) + 2ull * C) * sizeof(float);
+  return (coop_k_offset(PL, C, B, groups) + coop_tail_floats(groups) + 2ull * C) * sizeof(float);
 }
 
 GroupPlan two_phase_plan(const SkipGroupCall& c) {
@@ -199,7 +200,7 @@ static bool plan_coop_l2_route(const SkipGroupCall& c, bool vector_ok, GroupPlan
   const int PL = static_cast<int>(kL2MaxThreads / (c.C / ve));
   const int block = static_cast<int>(PL * (c.C / ve));
   const size_t smem = static_cast<size_t>(c.C) * sizeof(float4) +
-                      static_cast<size_t>(c.groups) * sizeof(float);
+                      static_cast<size_t>(2 * c.groups) * sizeof(float);
   int per_sm = 0;
   if (!fn || !allow_smem(fn, smem, dev) ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, block, smem) != cudaSuccess) {
@@ -340,7 +341,7 @@ static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, i
     const int PL = static_cast<int>(kCoopMaxThreads / CV);
     const int block = static_cast<int>(PL * CV);
     const size_t smem1 = coop_smem_bytes(PL, static_cast<int>(c.C), 0, c.groups);
-    for (int nv : {1, 2, 4, 8}) {
+    for (int nv : {1, 2, 3, 4, 5, 6, 8}) {
       void* fn = pick_coop_any(c.t, c.m, ve, nv);
       if (!fn) continue;
       // dynamic + static shared memory must fit the per-block opt-in limit
