@@ -223,17 +223,27 @@ B200NORM_API b200norm_status b200norm_skip_group(
  * Arguments and results are those of b200norm_skip_group without
  * `workspace` / `workspace_bytes`.  Instead the library uses a fixed scratch
  * array of 256 + 2 MiB bytes in device memory, which every GPU that loads
- * the library holds until the process exits.  That covers up to 64 groups
- * on every route; a shape that needs more returns B200NORM_ERR_UNSUPPORTED
- * (see b200norm_last_error) and enqueues nothing -- use b200norm_skip_group
- * with a workspace for it.  No call allocates or frees memory.
+ * the library holds until the process exits.  A call fits exactly when
+ * b200norm_skip_group_workspace_size() of its shape is at most that size;
+ * with L = C / groups * H * W, NHWC shapes with at most 32 groups and
+ * N * ceil(L / 4096) <= 4,096 fit, and NCHW shapes fit when
+ * N * groups * ceil(L / 4096) <= 131,072.  A larger shape returns
+ * B200NORM_ERR_UNSUPPORTED (see b200norm_last_error); use
+ * b200norm_skip_group with a workspace for it.  Every argument is checked
+ * before anything is enqueued, as for b200norm_skip_group: a call that
+ * returns an error has enqueued nothing.  No call allocates or frees memory.
  *
  *   - The first call on a device looks up the scratch array's device address
- *     (cudaGetSymbolAddress) with that device current.  Make that first call
- *     before any stream capture begins.
- *   - Each call clears the array's 256-byte control block on `stream` before
- *     its kernels; the rest keeps the previous call's contents and is always
- *     written before it is read.
+ *     (cudaGetSymbolAddress) with that device current, and keeps it for the
+ *     life of the process: make that first call before any stream capture
+ *     begins, and do not use the library across a cudaDeviceReset().
+ *   - Each call clears the scratch's barrier counters on `stream` before its
+ *     kernels; the slots keep the previous call's contents and are always
+ *     written before they are read.
+ *   - A bounded device-side wait that gives up (see b200norm_skip_group)
+ *     records B200NORM_ERR_DEVICE_TIMEOUT in the scratch, where it stays,
+ *     through later calls, until b200norm_skip_group_noalloc_status() reads
+ *     and clears it.
  *   - All calls on a device share the one array: calls whose work overlaps on
  *     the GPU (different streams without ordering between them) race and give
  *     undefined results.  Order them, e.g. issue them on one stream.
@@ -243,6 +253,13 @@ B200NORM_API b200norm_status b200norm_skip_group_noalloc(
     const void* gamma, const void* beta, void* y, void* s, int64_t N, int64_t C, int64_t H,
     int64_t W, b200norm_dtype T, b200norm_dtype M, int groups, float epsilon, int activation,
     int channels_last, b200norm_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the device-side error record of
+ * b200norm_skip_group_noalloc's scratch on the current device: B200NORM_OK,
+ * or B200NORM_ERR_DEVICE_TIMEOUT if a bounded wait of an earlier call gave up
+ * (that call's outputs are undefined).  B200NORM_ERR_CUDA if the copy failed.
+ * Allocates nothing. */
+B200NORM_API b200norm_status b200norm_skip_group_noalloc_status(b200norm_stream_t stream);
 
 /* Zero-fill a SkipGroupNorm workspace (cudaMemsetAsync on `stream`). */
 B200NORM_API b200norm_status b200norm_workspace_init(void* workspace, size_t workspace_bytes,

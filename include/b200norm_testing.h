@@ -22,6 +22,14 @@ B200NORM_API b200norm_status b200norm_testing_barrier_timeout(void* workspace,
                                                               uint64_t limit_ns,
                                                               b200norm_stream_t stream);
 
+/* The same probe on the static scratch of b200norm_skip_group_noalloc (on the
+ * current device): its waits give up after `limit_ns` and record
+ * B200NORM_ERR_DEVICE_TIMEOUT there, which
+ * b200norm_skip_group_noalloc_status() then reports and clears.  The barrier
+ * counts are back at zero afterwards.  Never faults. */
+B200NORM_API b200norm_status b200norm_testing_noalloc_barrier_timeout(uint64_t limit_ns,
+                                                                      b200norm_stream_t stream);
+
 /* Force a schedule on the calling thread (0 = automatic choice):
  *   row_mode:    1 = register-resident schedules only (never the pipelined
  *                    one that automatic choice gives long runs of short

@@ -24,8 +24,8 @@ import threading
 import torch
 
 __all__ = ["skip_rms", "skip_rms_stats", "gated_rms", "skip_group", "workspace_size",
-           "workspace_init", "workspace_status", "library", "library_path", "B200NormError",
-           "SSLN_EPS_DEFAULT"]
+           "workspace_init", "workspace_status", "noalloc_status", "rows_status", "library",
+           "library_path", "B200NormError", "SSLN_EPS_DEFAULT"]
 
 # float32(1e-12): SkipSimplifiedLayerNormalization README, Attributes, epsilon.
 SSLN_EPS_DEFAULT = 9.999999960041972e-13
@@ -75,10 +75,15 @@ def library() -> ctypes.CDLL:
             "b200norm_skip_group": ([vp, vp, i32, ctypes.POINTER(ctypes.c_int64), vp, vp, vp,
                                      vp, vp, i64, i64, i64, i64, i32, i32, i32, f32, i32, i32,
                                      vp, sz, vp], i32),
+            "b200norm_skip_group_noalloc": ([vp, vp, i32, ctypes.POINTER(ctypes.c_int64), vp,
+                                             vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, i32,
+                                             f32, i32, i32, vp], i32),
+            "b200norm_skip_group_noalloc_status": ([vp], i32),
             "b200norm_workspace_init": ([vp, sz, vp], i32),
             "b200norm_workspace_status": ([vp, vp], i32),
             "b200norm_rows_status": ([vp], i32),
             "b200norm_testing_barrier_timeout": ([vp, sz, ctypes.c_uint64, vp], i32),
+            "b200norm_testing_noalloc_barrier_timeout": ([ctypes.c_uint64, vp], i32),
             "b200norm_testing_force": ([i32, i32], i32),
             "b200norm_testing_force_split": ([i32, i32], i32),
             "b200norm_testing_set_pdl": ([i32], i32),
@@ -108,9 +113,12 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _torch_stream(device, stream):
+    return stream if stream is not None else torch.cuda.current_stream(device)
+
+
 def _stream(device, stream):
-    s = stream if stream is not None else torch.cuda.current_stream(device)
-    return ctypes.c_void_p(s.cuda_stream)
+    return ctypes.c_void_p(_torch_stream(device, stream).cuda_stream)
 
 
 def _cuda(name, t, device=None, dtype=None):
@@ -230,6 +238,16 @@ def rows_status(stream=None, device=None):
         _check(library().b200norm_rows_status(_stream(dev, stream)))
 
 
+def noalloc_status(stream=None, device=None):
+    """Synchronizes ``stream`` and raises B200NormError if a bounded
+    device-side wait of an allocation-free SkipGroupNorm call
+    (``b200norm_skip_group_noalloc``) on the device gave up since the last
+    call; the record is then cleared."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        _check(library().b200norm_skip_group_noalloc_status(_stream(dev, stream)))
+
+
 def workspace_size(N, C, H, W, groups, dtype=torch.float16, channels_last=1) -> int:
     return int(library().b200norm_skip_group_workspace_size(N, C, H, W, groups, _DTYPES[dtype],
                                                             1 if channels_last else 0))
@@ -245,14 +263,18 @@ def workspace_status(ws, stream=None):
     _check(library().b200norm_workspace_status(_ptr(ws), _stream(ws.device, stream)))
 
 
-def _workspace_for(device, stream_handle, nbytes):
+def _workspace_for(device, stream, nbytes):
     """A zero-filled workspace cached per (device, stream); calls on one
-    stream are serialized, so they may share it."""
-    key = (device.index, stream_handle)
+    stream are serialized, so they may share it.  It is allocated and zeroed
+    on that stream, so the clear is ordered before the kernels that use it,
+    and a smaller one it replaces goes back to the caching allocator on the
+    stream its kernels ran on (its allocation stream)."""
+    key = (device.index, stream.cuda_stream)
     with _ws_lock:
         ws = _workspaces.get(key)
         if ws is None or ws.numel() < nbytes:
-            ws = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
+            with torch.cuda.stream(stream):
+                ws = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
             _workspaces[key] = ws
         return ws
 
@@ -282,10 +304,11 @@ def skip_group(x, skip, gamma, beta, bias=None, *, groups, activation, epsilon=1
         raise ValueError("gamma, beta and bias must have C elements")
     out = _out("Y", y, x)
     ssum = _out("S", s, x) if want_sum or s is not None else None
-    st = _stream(dev, stream)
+    tst = _torch_stream(dev, stream)
+    st = ctypes.c_void_p(tst.cuda_stream)
     nbytes = workspace_size(N, C, H, W, groups, dt, cl)
     if workspace is None:
-        workspace = _workspace_for(dev, st.value, nbytes)
+        workspace = _workspace_for(dev, tst, nbytes)
     if skip.dim() > 4:
         raise ValueError("skip must have X's shape, (N, C) or (N, 1, 1, C)")
     dims = (ctypes.c_int64 * 4)(*([int(d) for d in skip.shape] + [0] * (4 - skip.dim())))

@@ -200,6 +200,52 @@ void set_pdl_enabled(bool on) { g_pdl.store(on, std::memory_order_relaxed); }
 
 void b200norm::set_error_message(const char* msg) { g_error = msg; }
 
+b200norm_status b200norm::skip_group_check(const void* x, const void* skip, int skip_rank,
+                                           const int64_t* skip_dims, const void* bias,
+                                           const void* gamma, const void* beta, const void* y,
+                                           const void* s, int64_t N, int64_t C, int64_t H,
+                                           int64_t W, b200norm_dtype T, b200norm_dtype M,
+                                           int groups, float epsilon, int activation,
+                                           int channels_last, bool* nothing_to_do) {
+  *nothing_to_do = false;
+  if (!group_types_ok(T, M))
+    return fail(B200NORM_ERR_UNSUPPORTED, "element types T=%d M=%d not supported", T, M);
+  if (N < 0 || C <= 0 || H < 0 || W < 0)
+    return fail(B200NORM_ERR_INVALID_ARGUMENT, "need N >= 0, C > 0, H >= 0, W >= 0");
+  if (groups <= 0 || C % groups != 0)
+    return fail(B200NORM_ERR_INVALID_ARGUMENT, "groups (%d) must be > 0 and divide C (%lld)",
+                groups, static_cast<long long>(C));
+  if (activation != 0 && activation != 1)
+    return fail(B200NORM_ERR_INVALID_ARGUMENT, "activation must be 0 (none) or 1 (SiLU)");
+  if (b200norm_status st = check_eps(epsilon)) return st;
+  const bool cl = channels_last != 0;
+  const int bc = classify_skip(skip_rank, skip_dims, N, C, H, W, cl);
+  if (bc < 0)
+    return fail(B200NORM_ERR_INVALID_ARGUMENT,
+                "skip must have X's shape, (N, C) or (N, 1, 1, C)");
+  if (N == 0 || H == 0 || W == 0) {
+    *nothing_to_do = true;
+    return B200NORM_OK;
+  }
+  if (C > 0x7fffffffLL || H * W > 0x7fffffffLL || N > 0x7fffffffLL)
+    return fail(B200NORM_ERR_UNSUPPORTED, "C, H*W or N exceeds 2^31-1");
+  if (!x || !skip || !gamma || !beta || !y)
+    return fail(B200NORM_ERR_INVALID_ARGUMENT, "x, skip, gamma, beta and y are required");
+  const size_t es = dtype_size(to_dtype(T)), ms = dtype_size(to_dtype(M));
+  const void* tptrs[] = {x, skip, bias, y, s};
+  for (const void* p : tptrs)
+    if (p && !aligned(p, es))
+      return fail(B200NORM_ERR_INVALID_ARGUMENT, "tensor pointer not aligned to its element size");
+  if (!aligned(gamma, ms) || !aligned(beta, ms))
+    return fail(B200NORM_ERR_INVALID_ARGUMENT, "gamma/beta not aligned to their element size");
+  const size_t tb = static_cast<size_t>(N * C * H * W) * es;
+  const size_t sb = bc ? static_cast<size_t>(N * C) * es : tb;
+  const Range in[] = {{x, tb, "X"}, {skip, sb, "skip"}, {bias, C * es, "bias"},
+                      {gamma, C * ms, "gamma"}, {beta, C * ms, "beta"}};
+  const Range out[] = {{y, tb, "Y"}, {s, tb, "S"}};
+  return check_overlaps(in, 5, out, 2);
+}
+
 extern "C" {
 
 int b200norm_version(void) { return 1; }
@@ -278,9 +324,9 @@ b200norm_status b200norm_gated_rms(const void* x, const void* gate, const void* 
 }
 
 size_t b200norm_skip_group_workspace_size(int64_t N, int64_t C, int64_t H, int64_t W, int groups,
-                                          b200norm_dtype T, int /*channels_last*/) {
+                                          b200norm_dtype T, int channels_last) {
   if (!dtype_ok(T)) return kControlBytes;
-  return group_workspace_bytes(N, C, H, W, groups, to_dtype(T));
+  return group_workspace_bytes(N, C, H, W, groups, to_dtype(T), channels_last != 0);
 }
 
 b200norm_status b200norm_skip_group(const void* x, const void* skip, int skip_rank,
@@ -291,50 +337,35 @@ b200norm_status b200norm_skip_group(const void* x, const void* skip, int skip_ra
                                     float epsilon, int activation, int channels_last,
                                     void* workspace, size_t workspace_bytes,
                                     b200norm_stream_t stream) {
-  if (!group_types_ok(T, M))
-    return fail(B200NORM_ERR_UNSUPPORTED, "element types T=%d M=%d not supported", T, M);
-  if (N < 0 || C <= 0 || H < 0 || W < 0)
-    return fail(B200NORM_ERR_INVALID_ARGUMENT, "need N >= 0, C > 0, H >= 0, W >= 0");
-  if (groups <= 0 || C % groups != 0)
-    return fail(B200NORM_ERR_INVALID_ARGUMENT, "groups (%d) must be > 0 and divide C (%lld)",
-                groups, static_cast<long long>(C));
-  if (activation != 0 && activation != 1)
-    return fail(B200NORM_ERR_INVALID_ARGUMENT, "activation must be 0 (none) or 1 (SiLU)");
-  if (b200norm_status st = check_eps(epsilon)) return st;
+  bool nothing_to_do = false;
+  if (b200norm_status st = skip_group_check(x, skip, skip_rank, skip_dims, bias, gamma, beta, y,
+                                            s, N, C, H, W, T, M, groups, epsilon, activation,
+                                            channels_last, &nothing_to_do))
+    return st;
+  if (nothing_to_do) return ok();
   const bool cl = channels_last != 0;
-  const int bc = classify_skip(skip_rank, skip_dims, N, C, H, W, cl);
-  if (bc < 0)
-    return fail(B200NORM_ERR_INVALID_ARGUMENT,
-                "skip must have X's shape, (N, C) or (N, 1, 1, C)");
-  if (N == 0 || H == 0 || W == 0) return ok();
-  if (C > 0x7fffffffLL || H * W > 0x7fffffffLL || N > 0x7fffffffLL)
-    return fail(B200NORM_ERR_UNSUPPORTED, "C, H*W or N exceeds 2^31-1");
-  if (!x || !skip || !gamma || !beta || !y)
-    return fail(B200NORM_ERR_INVALID_ARGUMENT, "x, skip, gamma, beta and y are required");
-  const size_t need = group_workspace_bytes(N, C, H, W, groups, to_dtype(T));
+  const size_t need = group_workspace_bytes(N, C, H, W, groups, to_dtype(T), cl);
   if (!workspace || workspace_bytes < need)
     return fail(B200NORM_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu at %p)", need,
                 workspace_bytes, workspace);
   if (!aligned(workspace, 256))
     return fail(B200NORM_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   const size_t es = dtype_size(to_dtype(T)), ms = dtype_size(to_dtype(M));
-  const void* tptrs[] = {x, skip, bias, y, s};
-  for (const void* p : tptrs)
-    if (p && !aligned(p, es))
-      return fail(B200NORM_ERR_INVALID_ARGUMENT, "tensor pointer not aligned to its element size");
-  if (!aligned(gamma, ms) || !aligned(beta, ms))
-    return fail(B200NORM_ERR_INVALID_ARGUMENT, "gamma/beta not aligned to their element size");
+  const int bc = classify_skip(skip_rank, skip_dims, N, C, H, W, cl);
   const size_t tb = static_cast<size_t>(N * C * H * W) * es;
   const size_t sb = bc ? static_cast<size_t>(N * C) * es : tb;
-  const Range in[] = {{x, tb, "X"}, {skip, sb, "skip"}, {bias, C * es, "bias"},
-                      {gamma, C * ms, "gamma"}, {beta, C * ms, "beta"},
-                      {workspace, workspace_bytes, "workspace"}};
-  const Range out[] = {{y, tb, "Y"}, {s, tb, "S"}};
-  if (b200norm_status st = check_overlaps(in, 6, out, 2)) return st;
+  const Range ws = {workspace, workspace_bytes, "workspace"};
+  const Range others[] = {{x, tb, "X"}, {skip, sb, "skip"}, {bias, C * es, "bias"},
+                          {gamma, C * ms, "gamma"}, {beta, C * ms, "beta"}, {y, tb, "Y"},
+                          {s, tb, "S"}};
+  for (const Range& r : others)
+    if (overlaps(ws, r))
+      return fail(B200NORM_ERR_WORKSPACE, "workspace overlaps %s", r.name);
 
   SkipGroupCall c{x, skip, bias, gamma, beta, y, s, N, C, H, W, groups, to_dtype(T), to_dtype(M),
                   bc == 1, activation, cl, epsilon, workspace, workspace_bytes};
   bool vec = true;
+  const void* tptrs[] = {x, skip, bias, y, s};
   for (const void* p : tptrs)
     if (p && !aligned(p, 16)) vec = false;
   GroupPlan plan;

@@ -32,18 +32,23 @@ static bool l2_route_ok(int64_t N, int64_t C, int ve, int64_t in_bytes) {
          in_bytes <= kL2RouteMaxBytes;
 }
 
-size_t group_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int groups, DType t) {
+size_t group_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int groups, DType t,
+                             bool channels_last) {
   if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || groups <= 0) return kControlBytes;
   const int64_t L = (C / groups) * H * W;
-  const int64_t two_phase = N * groups * cdiv(L, kTwoPhaseChunk);
-  const int64_t coop = static_cast<int64_t>(kMaxCoopCtas) * groups;
-  int64_t slots = two_phase > coop ? two_phase : coop;
-  const int64_t es = static_cast<int64_t>(dtype_size(t));
-  for (int ve : {1, static_cast<int>(16 / es)}) {
-    // route 4: at most kMaxCoopCtas partials per group, then the statistics
-    if (l2_route_ok(N, C, ve, N * H * W * C * es)) {
-      const int64_t r4 = static_cast<int64_t>(kMaxCoopCtas) * groups + N * groups;
-      if (r4 > slots) slots = r4;
+  // route 3 (either layout): one piece per chunk of every group instance;
+  // route 1 (NCHW) needs no slots
+  int64_t slots = N * groups * cdiv(L, kTwoPhaseChunk);
+  if (channels_last) {
+    // routes 2 and 5: one piece per CTA and group, at most kMaxCoopCtas CTAs
+    slots = std::max<int64_t>(slots, static_cast<int64_t>(kMaxCoopCtas) * groups);
+    const int64_t es = static_cast<int64_t>(dtype_size(t));
+    for (int ve : {1, static_cast<int>(16 / es)}) {
+      // route 4: the pieces, then the statistics of every instance
+      if (l2_route_ok(N, C, ve, N * H * W * C * es)) {
+        const int64_t r4 = static_cast<int64_t>(kMaxCoopCtas) * groups + N * groups;
+        if (r4 > slots) slots = r4;
+      }
     }
   }
   return kControlBytes + static_cast<size_t>(slots) * sizeof(float4);

@@ -10,6 +10,8 @@
 
 #include <mutex>
 
+#include "b200norm.h"
+
 namespace b200norm {
 
 // A small thread-safe cache of launch decisions keyed by a plain struct
@@ -173,7 +175,20 @@ constexpr size_t kControlBytes = 256;
 constexpr int kTwoPhaseChunk = 4096;   // elements per CTA in route 3
 constexpr int kMaxCoopCtas = 2048;     // upper bound of route-2 grids
 
-size_t group_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int groups, DType t);
+// Workspace a SkipGroupNorm call needs: the control block, then the slots of
+// every route that can take the shape in its layout (NCHW: the two-phase
+// route's chunks; NHWC also the cooperative and L2 routes' pieces).
+size_t group_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int groups, DType t,
+                             bool channels_last);
+// Every argument check of b200norm_skip_group except those of the workspace,
+// made before anything is enqueued (the message goes to b200norm_last_error);
+// B200NORM_OK with *nothing_to_do set when N, H or W is zero.
+b200norm_status skip_group_check(const void* x, const void* skip, int skip_rank,
+                                 const int64_t* skip_dims, const void* bias, const void* gamma,
+                                 const void* beta, const void* y, const void* s, int64_t N,
+                                 int64_t C, int64_t H, int64_t W, b200norm_dtype T,
+                                 b200norm_dtype M, int groups, float epsilon, int activation,
+                                 int channels_last, bool* nothing_to_do);
 // force_route 0 picks the route; 2, 3 or 4 asks for that route and returns
 // cudaErrorNotSupported when it cannot take the call.
 cudaError_t plan_group(const SkipGroupCall& c, bool vector_ok, int force_route, GroupPlan* plan);

@@ -141,12 +141,56 @@ def test_skip_group_validation(lib):
 
 
 def test_workspace_size_covers_every_route(lib):
-    # the workspace holds a control block plus one 16-byte moment slot per
-    # partial of the largest route
+    # the workspace holds a control block plus one 16-byte slot per piece of
+    # the largest route the layout can take
     small = lib.b200norm_skip_group_workspace_size(2, 320, 64, 64, 32, F16, 1)
     assert small >= 256 + 16 * 32
     big = lib.b200norm_skip_group_workspace_size(1, 64, 1024, 1024, 1, F16, 0)
     assert big >= 256 + 16 * ((64 * 1024 * 1024 + 4095) // 4096)
+
+
+def test_workspace_size_follows_the_layout(lib):
+    # NCHW calls run the resident route (no slots) or the two-phase route
+    # (one slot per 4,096-element chunk of every group instance); NHWC calls
+    # can also take the cooperative and L2 routes (up to 2,048 CTAs' pieces
+    # per group, and the L2 route's statistics)
+    nchw = lib.b200norm_skip_group_workspace_size(16, 1280, 16, 16, 32, F32, 0)
+    assert nchw == 256 + 16 * (16 * 32 * 3)
+    nhwc = lib.b200norm_skip_group_workspace_size(16, 1280, 16, 16, 32, F32, 1)
+    assert nhwc >= 256 + 16 * 2048 * 32
+    # any non-zero channels_last means NHWC
+    assert lib.b200norm_skip_group_workspace_size(16, 1280, 16, 16, 32, F32, 7) == nhwc
+
+
+def noalloc(lib, **kw):
+    a = dict(x=FAKE, skip=FAKE + (1 << 30), rank=2, dims=(2, 8, 0, 0), bias=None,
+             gamma=FAKE + (2 << 30), beta=FAKE + (2 << 30) + 4096, y=FAKE + (3 << 30), s=None,
+             N=2, C=8, H=3, W=2, T=F16, M=F32, groups=2, eps=1e-5, act=0, cl=1)
+    a.update(kw)
+    dims = (ctypes.c_int64 * 4)(*a["dims"])
+    return lib.b200norm_skip_group_noalloc(a["x"], a["skip"], a["rank"], dims, a["bias"],
+                                           a["gamma"], a["beta"], a["y"], a["s"], a["N"], a["C"],
+                                           a["H"], a["W"], a["T"], a["M"], a["groups"], a["eps"],
+                                           a["act"], a["cl"], None)
+
+
+def test_noalloc_refuses_before_touching_a_device(lib):
+    """The allocation-free entry makes the regular entry's argument checks
+    and its own size check before any CUDA call (none of these reach a GPU)."""
+    assert noalloc(lib, groups=3) == INVALID
+    assert noalloc(lib, act=2) == INVALID
+    assert noalloc(lib, eps=float("nan")) == INVALID
+    assert noalloc(lib, M=2) == UNSUPPORTED
+    assert noalloc(lib, rank=4, dims=(2, 3, 2, 4)) == INVALID
+    assert noalloc(lib, y=FAKE + 2) == INVALID                      # aliases X
+    assert noalloc(lib, y=None) == INVALID
+    assert noalloc(lib, N=0, dims=(0, 8, 0, 0), x=None, skip=None, y=None) == OK  # empty
+    # 64 groups of a small NHWC shape the L2 route could take: more slots than
+    # the 256 + 2 MiB scratch holds
+    dims64 = (2, 64, 0, 0)
+    assert noalloc(lib, C=64, H=8, W=8, groups=64, dims=dims64, cl=1) == UNSUPPORTED
+    assert b"static scratch" in lib.b200norm_last_error()
+    assert lib.b200norm_skip_group_workspace_size(2, 64, 8, 8, 64, F16, 1) > 256 + (2 << 20)
 
 
 def plan_rows(lib, rows, n, T, aligned=1):

@@ -1,7 +1,10 @@
 """The C ABI from a plain C program (tests/c/abi_example.c): compiled against
 include/b200norm.h and linked to the in-tree libb200norm.so, with no Python in
 the call path.  The CPU test runs the argument-error paths; the GPU test also
-runs SkipSimplifiedLayerNormalization on a closed-form case."""
+runs every operator on a closed-form case on the README usage examples'
+shapes: SkipSimplifiedLayerNormalization, GatedRMSNorm with C = 1, and
+SkipGroupNorm through a workspace sized by
+b200norm_skip_group_workspace_size() and through the allocation-free entry."""
 import os
 import shutil
 import subprocess
@@ -37,7 +40,7 @@ def test_c_caller_argument_errors(tmp_path):
 
 
 @pytest.mark.gpu
-def test_c_caller_runs_skip_rms(tmp_path):
+def test_c_caller_runs_every_operator(tmp_path):
     b2.library()
     exe = _build(tmp_path, gpu=True)
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)

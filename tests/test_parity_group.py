@@ -264,3 +264,25 @@ def test_any_nonzero_channels_last_means_nhwc(flag):
                                activation=1, channels_last=1)
     assert_bitexact(to_host(s), rs)
     assert_y_close(to_host(y), ry)
+
+
+def test_cached_workspace_on_a_non_current_stream():
+    """skip_group(stream=s) without an explicit workspace: the binding makes
+    and clears its cached workspace on s itself (so the clear is ordered
+    before the kernels on s), and replaces it on s when a larger shape needs
+    more; results match the oracle on both shapes."""
+    side = torch.cuda.Stream()
+    cur = torch.cuda.current_stream()
+    for shape, G in (((2, 16, 16, 64), 8), ((2, 64, 64, 320), 32)):
+        d = synthetic.skip_group_inputs(shape, np.float16, np.float32, seed=61, channels_last=1,
+                                        skip="nc", bias=True)
+        t = {k: to_dev(v) for k, v in d.items()}
+        side.wait_stream(cur)
+        y, s = b2.skip_group(t["x"], t["skip"], t["gamma"], t["beta"], t["bias"], groups=G,
+                             activation=1, channels_last=1, want_sum=True, stream=side)
+        cur.wait_stream(side)
+        torch.cuda.synchronize()
+        ry, rs = oracle.skip_group(d["x"], d["skip"], d["gamma"], d["beta"], d["bias"],
+                                   groups=G, activation=1, channels_last=1)
+        assert_bitexact(to_host(s), rs)
+        assert_y_close(to_host(y), ry)
