@@ -44,6 +44,8 @@ BF16_WORKLOADS = ["ssln_bf16_8x2048x4096", "gated_bf16_4x4096x8192_c128",
                   "sgn_nhwc_bf16_2x64x64x320", "sgn_nchw_bf16_16x1280x16x16"]
 # short SkipSimplifiedLayerNormalization rows: the pipelined bulk-copy schedule
 SHORT_WORKLOADS = ["ssln_fp32_262144x128"]
+# the small SkipSimplifiedLayerNormalization batch: latency-bound, timed on its own
+SMALL_WORKLOADS = ["ssln_fp32_64x768"]
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -139,19 +141,26 @@ def host_tensor(torch, a):
     return torch.from_numpy(a)
 
 
+def l2_bytes(torch, dev):
+    try:
+        return int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    except (AttributeError, RuntimeError):
+        return 129 * 2**20
+
+
 def make_calls(torch, b2, dev, names=None, rotate=True):
     """Device inputs, preallocated outputs and call closures per workload.
 
-    With `rotate`, each workload gets `nsets` independent input/output sets;
-    the per-operator timing cycles through them so that the inputs it reads
-    (at least 4 x 129 MB of traffic between two uses of a set) come from HBM,
-    not from L2.  Without it there is one set (decode-shaped calls, whose
-    inputs a preceding kernel has just written)."""
+    With `rotate`, each workload gets `nsets` independent input/output sets,
+    enough that the other sets move at least 3 x L2 of traffic between two
+    uses of one set; the per-operator timing cycles through them, so the
+    inputs it reads come from HBM, not from L2.  Without it there is one set
+    (latency-bound calls, whose inputs a preceding kernel has just written)."""
     calls = []
+    l2 = l2_bytes(torch, dev)
     for name in (STEP_WORKLOADS if names is None else names):
         spec, d = synthetic.workload(name)
-        nsets = max(1, -(-4 * 129_000_000 // synthetic.algorithmic_bytes(name)))
-        nsets = min(nsets, 8) if rotate else 1
+        nsets = 1 + -(-3 * l2 // synthetic.algorithmic_bytes(name)) if rotate else 1
         fns, sets = [], []
         for _ in range(nsets):
             t = {k: (None if v is None else host_tensor(torch, v).to(dev)) for k, v in d.items()}
@@ -213,11 +222,16 @@ def job_gbs(step_bytes, world, ms_per_step):
     return step_bytes * world / (ms_per_step * 1e-3) / 1e9
 
 
+OP_MIN_LAUNCHES = 100  # per operator, over all timed replays
+OP_MIN_ROUNDS = 10     # timed replays per operator (median and best over them)
+
+
 def op_graphs_of(torch, calls, stream):
-    """One graph per workload: 4 x nsets calls cycling through its sets."""
+    """One graph per workload: 2 x nsets calls cycling through its sets (at
+    least 8)."""
     graphs, reps = [], []
     for c in calls:
-        rep = 4 * len(c["fns"])
+        rep = max(8, 2 * len(c["fns"]))
         def many(c=c, rep=rep):
             for r in range(rep):
                 c["fns"][r % len(c["fns"])]()
@@ -226,13 +240,15 @@ def op_graphs_of(torch, calls, stream):
     return graphs, reps
 
 
-def time_op_graphs(torch, graphs, reps, rounds, stream):
-    """Milliseconds per call of each workload over `rounds` back-to-back
-    replays of its graph (after one untimed replay), with an event between
-    consecutive replays: (mean, median, best) per workload.  The mean is the
-    whole run's time over its calls."""
+def time_op_graphs(torch, graphs, reps, stream):
+    """Milliseconds per call of each workload over back-to-back replays of
+    its graph (after one untimed replay) -- at least OP_MIN_ROUNDS replays and
+    OP_MIN_LAUNCHES calls -- with an event between consecutive replays:
+    (mean, median, best, calls) per workload.  The mean is the whole run's
+    time over its calls; median and best are over the replays."""
     out = []
     for g, rep in zip(graphs, reps):
+        rounds = max(OP_MIN_ROUNDS, -(-OP_MIN_LAUNCHES // rep))
         g.replay()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(rounds + 1)]
         ev[0].record(stream)
@@ -242,22 +258,22 @@ def time_op_graphs(torch, graphs, reps, rounds, stream):
         torch.cuda.synchronize()
         per = np.array([ev[k].elapsed_time(ev[k + 1]) / rep for k in range(rounds)])
         out.append((ev[0].elapsed_time(ev[rounds]) / (rounds * rep), float(np.median(per)),
-                    float(per.min())))
+                    float(per.min()), rounds * rep))
     return out
 
 
+UNIT_NAMES = {"skip_rms": "rows", "gated_rms": "C-spans", "skip_group": "group instances"}
+
+
 def op_entry(c, t):
-    ms, med, best = t
+    ms, med, best, n = t
     peak, _ = peak_hbm()
     gbs = c["bytes"] / (ms * 1e-3) / 1e9
-    return {"us_per_call": round(ms * 1e3, 3), "us_per_call_median": round(med * 1e3, 3),
-            "us_per_call_best": round(best * 1e3, 3), "GB_s": round(gbs, 1),
-            "frac_of_measured_peak": round(gbs / peak, 4),
-            "frac_of_8TBs_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
-            "units_per_s": round(c["units"] / (ms * 1e-3), 1),
-            "units": {"skip_rms": "rows", "gated_rms": "C-spans",
-                      "skip_group": "group instances"}[c["spec"]["op"]],
-            "algorithmic_bytes": c["bytes"]}
+    return {"us_per_call": round(ms * 1e3, 3), "us_median": round(med * 1e3, 3),
+            "us_best": round(best * 1e3, 3), "GB_s": round(gbs, 1),
+            "of_measured_peak": round(gbs / peak, 4), "of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
+            "units_per_s": float(f"{c['units'] / (ms * 1e-3):.4g}"),
+            "units": UNIT_NAMES[c["spec"]["op"]], "sets": len(c["fns"]), "calls": n}
 
 
 def launches_per_call(b2, spec):
@@ -337,13 +353,10 @@ def run_ours(args, rank, world, dist):
     t_wall1 = time.time()
     if dist:
         dist.barrier()
-    time.sleep(0.1)
-    clocks.stop()
     total_ms = max_over_ranks(torch, dist, start.elapsed_time(end), dev)
 
     # --- per-operator launch durations (events around each operator graph) --
-    op_rounds = max(3, min(50, args.steps // 20))
-    per_call_ms = time_op_graphs(torch, op_graphs, reps, op_rounds, stream)
+    per_call_ms = time_op_graphs(torch, op_graphs, reps, stream)
     del op_graphs
 
     # --- bfloat16 variants of the large workloads, timed the same way -------
@@ -355,7 +368,7 @@ def run_ours(args, rank, world, dist):
                 f()
         torch.cuda.synchronize()
         graphs, breps = op_graphs_of(torch, bcalls, cap)
-        bms = time_op_graphs(torch, graphs, breps, op_rounds, stream)
+        bms = time_op_graphs(torch, graphs, breps, stream)
         bf16_ops = {c["name"]: op_entry(c, ms) for c, ms in zip(bcalls, bms)}
         del graphs, bcalls
         torch.cuda.synchronize()
@@ -369,38 +382,44 @@ def run_ours(args, rank, world, dist):
                 f()
         torch.cuda.synchronize()
         graphs, sreps = op_graphs_of(torch, scalls, cap)
-        sms_ = time_op_graphs(torch, graphs, sreps, op_rounds, stream)
+        sms_ = time_op_graphs(torch, graphs, sreps, stream)
         short_ops = {c["name"]: op_entry(c, ms) for c, ms in zip(scalls, sms_)}
         del graphs, scalls
         torch.cuda.synchronize()
         b2.rows_status()
 
-    # --- decode-shaped calls: per-call time in a graph of back-to-back calls -
-    decode = {}
-    if not args.no_decode:
-        for c in make_calls(torch, b2, dev, DECODE_WORKLOADS, rotate=False):
+    # --- latency-bound calls: per-call time in a graph of back-to-back calls -
+    def latency_section(names):
+        out = {}
+        for c in make_calls(torch, b2, dev, names, rotate=False):
             rep = 200
             c["fn"]()
             torch.cuda.synchronize()
             g = capture(torch, lambda c=c, rep=rep: [c["fn"]() for _ in range(rep)], cap)
             g.replay()
-            best = float("inf")
-            for _ in range(5):
+            per = []
+            for _ in range(OP_MIN_ROUNDS):
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 g.replay()
                 e1.record(stream)
                 torch.cuda.synchronize()
-                best = min(best, e0.elapsed_time(e1) / rep)
-            decode[c["name"]] = {
-                "us_per_call": round(best * 1e3, 3),
-                "units_per_s": round(c["units"] / (best * 1e-3), 1),
-                "units": {"skip_rms": "rows", "gated_rms": "C-spans"}[c["spec"]["op"]],
+                per.append(e0.elapsed_time(e1) / rep)
+            best, med = min(per), float(np.median(per))
+            out[c["name"]] = {
+                "us_per_call": round(best * 1e3, 3), "us_median": round(med * 1e3, 3),
+                "units_per_s": float(f"{c['units'] / (best * 1e-3):.4g}"),
+                "units": UNIT_NAMES[c["spec"]["op"]],
                 "GB_s": round(c["bytes"] / (best * 1e-3) / 1e9, 1),
-                "algorithmic_bytes": c["bytes"]}
+                "algorithmic_bytes": c["bytes"], "calls": rep * OP_MIN_ROUNDS}
             del g
         torch.cuda.synchronize()
+        return out
+
+    # the small SkipSimplifiedLayerNormalization batch (fp32 64 x 768): latency-bound
+    small = {} if args.only else latency_section(SMALL_WORKLOADS)
+    decode = {} if args.no_decode else latency_section(DECODE_WORKLOADS)
 
     # --- end to end through the public API with host buffers ---------------
     e2e_steps = 0 if args.no_e2e else min(args.steps, 20)
@@ -465,6 +484,9 @@ def run_ours(args, rank, world, dist):
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / e2e_steps, dev)
 
+    t_gpu1 = time.time()
+    time.sleep(0.1)
+    clocks.stop()
     if rank != 0:
         return None
 
@@ -495,16 +517,18 @@ def run_ours(args, rank, world, dist):
             "launch": "one CUDA graph per step (one call of each operator), replayed K times; "
                       "per-operator times from graphs of repeated calls over rotating buffers",
         },
-        "per_op": per_op,
         "per_op_bf16": ({"timing": "as per_op; bfloat16 storage, same shapes; not part of "
                                    "`value`", **bf16_ops} if bf16_ops else None),
         "per_op_short_rows": ({"timing": "as per_op; short rows, which take the pipelined "
                                           "bulk-copy schedule; not part of `value`",
                                **short_ops} if short_ops else None),
-        "decode": ({"timing": "best of 5 replays of a CUDA graph of 200 back-to-back calls on "
-                              "one buffer set (inputs L2-resident, as when a preceding kernel "
-                              "has just written them); not part of `value`",
+        "decode": ({"timing": f"best and median of {OP_MIN_ROUNDS} replays of a CUDA graph of "
+                              "200 back-to-back calls on one buffer set (inputs L2-resident, as "
+                              "when a preceding kernel has just written them); not part of "
+                              "`value`",
                     **decode} if decode else None),
+        "small": ({"timing": "as decode: the small batch is latency-bound (rows/s); not part "
+                             "of `value`", **small} if small else None),
         "roofline": {"bound": "hbm", "kernel": dom_c["name"], "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": peak_src, "traffic": traffic,
@@ -514,7 +538,15 @@ def run_ours(args, rank, world, dist):
                  "steps": e2e_steps, "ms_per_step": round(e2e_ms, 3)} if e2e_steps else None),
         "gpu_launches": launches,
         "clocks": clocks.summary(t_wall0, t_wall1),
+        "clocks_all_timing": clocks.summary(t_wall0, t_gpu1),
         "source_digest": digest,
+        "per_op_timing": (f"each step workload alone: a CUDA graph of 2 x sets (>= 8) calls "
+                          f"cycling over `sets` input/output sets (>= 3 x L2 of other sets' "
+                          f"traffic between two uses of one), replayed >= {OP_MIN_ROUNDS} times "
+                          f"and >= {OP_MIN_LAUNCHES} calls with an event between replays; "
+                          f"us_per_call = mean (the roofline's launch duration), median and "
+                          f"best over the replays"),
+        "per_op": per_op,
     }
     return line
 
@@ -671,6 +703,11 @@ def main():
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()
             line["cpu_baseline_all_cores"] = cpu_baseline_all_cores()
+        # the step workloads' per-operator figures last: a reader keeping only
+        # the end of the line still has them
+        for k in ("per_op_timing", "per_op"):
+            if k in line:
+                line[k] = line.pop(k)
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()
