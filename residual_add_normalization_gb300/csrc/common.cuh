@@ -235,6 +235,25 @@ __device__ __forceinline__ float2 cta_sum2(float2 v, float2* red) {
   return red[32];
 }
 
+// The same with one barrier: every thread adds the warps' partials itself, in
+// warp order (the same bits in every thread).  `red` holds one float2 per
+// warp; a later call on the same `red` needs a barrier between the two.
+__device__ __forceinline__ float2 cta_sum2_1b(float2 v, float2* red) {
+  v.x = warp_sum(v.x);
+  v.y = warp_sum(v.y);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float2 t = make_float2(0.0f, 0.0f);
+  for (int w = 0; w < nwarps; ++w) {
+    const float2 u = red[w];
+    t.x += u.x;
+    t.y += u.y;
+  }
+  return t;
+}
+
 // ---------------------------------------------------------------------------
 // Thread-block clusters (distributed shared memory)
 // ---------------------------------------------------------------------------

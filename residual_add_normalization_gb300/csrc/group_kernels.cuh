@@ -290,6 +290,12 @@ static __device__ __noinline__ GStats merge_pieces_global(const float4* part, in
 constexpr int kNchwThreads = B200NORM_NCHW_THREADS;
 constexpr int kNchwUnroll = B200NORM_NCHW_UNROLL;
 
+// Byte offset of route 1's gamma / beta table in dynamic shared memory: past
+// `span` vectors of S, rounded up to 16 bytes.
+__host__ __device__ constexpr size_t nchw_gb_offset(int span, size_t vbytes) {
+  return (static_cast<size_t>(span) * vbytes + 15) & ~static_cast<size_t>(15);
+}
+
 template <typename T, typename M, int VE>
 __global__ void __launch_bounds__(kNchwThreads, B200NORM_NCHW_MINB)
 sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
@@ -298,7 +304,7 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
   using P = Pack<T, VE>;
   extern __shared__ float4 smem4[];
   P* sb = reinterpret_cast<P*>(smem4);
-  __shared__ float2 red2[33];
+  __shared__ float2 red2[kNchwThreads / 32];
   __shared__ float4 slot_piece;  // this CTA's piece, read by the cluster's CTAs
   const unsigned csize = cluster_size();
   const unsigned rank = csize > 1 ? cluster_rank() : 0u;
@@ -310,6 +316,17 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
   const int cnt = min(span, L / VE - v0);  // may be <= 0 for trailing ranks
   const int64_t base = (n * a.C + static_cast<int64_t>(g) * a.cpg) * a.HW + static_cast<int64_t>(v0) * VE;
   const int cbase = g * a.cpg;
+  // gamma and beta of the channels this CTA touches, loaded now and staged in
+  // shared memory (after S, at the next 16-byte boundary: a scalar-path S
+  // can end anywhere) before the reduction's barrier, so that the output
+  // loop does not wait for them
+  float2* s_gb = reinterpret_cast<float2*>(reinterpret_cast<char*>(smem4) +
+                                           nchw_gb_offset(span, sizeof(P)));
+  const int c_lo = cnt > 0 ? cbase + static_cast<int>(fdiv(static_cast<unsigned>(v0), vpc)) : 0;
+  const int nch = cnt > 0 ? cbase + static_cast<int>(fdiv(static_cast<unsigned>(v0 + cnt - 1), vpc)) - c_lo + 1 : 0;
+  float2 gb = make_float2(0.0f, 0.0f);
+  if (static_cast<int>(threadIdx.x) < nch)
+    gb = make_float2(to_f32(a.gamma[c_lo + threadIdx.x]), to_f32(a.beta[c_lo + threadIdx.x]));
 
   // reference R: four residual sums spread over this CTA's range; threads
   // that hold vectors take it right behind their first loads
@@ -361,7 +378,8 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
   // was far from the piece's mean (every thread holds the same sums, so the
   // branch is uniform)
   const float n_cta = static_cast<float>(max(cnt, 0) * VE);
-  float2 t2 = cta_sum2(make_float2(sum, sq), red2);
+  if (static_cast<int>(threadIdx.x) < nch) s_gb[threadIdx.x] = gb;  // published by the barrier below
+  float2 t2 = cta_sum2_1b(make_float2(sum, sq), red2);
   float4 piece = piece_from_sums(n_cta, R, t2.x, t2.y);
   if (piece_ill(piece)) {
     const float R2 = R + piece.z;
@@ -375,7 +393,8 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
         s2 = fmaf(d, d, s2);
       }
     }
-    t2 = cta_sum2(make_float2(s1, s2), red2);
+    __syncthreads();  // every thread has read red2 (one-barrier sums)
+    t2 = cta_sum2_1b(make_float2(s1, s2), red2);
     piece = piece_from_sums(n_cta, R2, t2.x, t2.y);
   }
   GStats st;
@@ -391,7 +410,8 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
   const float rstd = 1.0f / sqrtf(st.var + a.eps);
   for (int i = threadIdx.x; i < cnt; i += kNchwThreads) {
     const int c = cbase + static_cast<int>(fdiv(static_cast<unsigned>(v0 + i), vpc));
-    const float ga = to_f32(a.gamma[c]), be = to_f32(a.beta[c]);
+    const float2 gbc = s_gb[c - c_lo];
+    const float ga = gbc.x, be = gbc.y;
     const P sv = sb[i];
     P out;
 #pragma unroll

@@ -319,7 +319,10 @@ static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, i
       return cudaSuccess;
     }
     const int span = static_cast<int>(cdiv(nvec, cs));
-    const size_t smem = static_cast<size_t>(span) * vbytes;
+    // S, then gamma / beta of the channels a CTA touches (a run of `span`
+    // vectors covers at most span / (H*W / ve) + 2 channels)
+    const size_t smem = nchw_gb_offset(span, static_cast<size_t>(vbytes)) +
+                        static_cast<size_t>(span / (HW / ve) + 2) * sizeof(float2);
     void* fn = pick_resident_any(c.t, c.m, ve);
     if (fn && allow_smem(fn, smem, dev) &&
         (cs == 1 || resident_cluster_fits(fn, kNchwThreads, static_cast<int>(cs), smem)) &&
