@@ -42,10 +42,10 @@ def sources():
 # The sources each kernel family is built from (for digests that identify one
 # family's code, e.g. to key profiler counters taken on it).
 FAMILY_SOURCES = {
-    "rows": ("common.cuh", "launch.h", "rows.cuh", "rows_launch.cuh", "rows_ops.cuh",
+    "rows": ("common.cuh", "bulk.cuh", "launch.h", "rows.cuh", "rows_launch.cuh", "rows_ops.cuh",
              "rows_pipe.cuh", "rows_gated.cu", "rows_ssln_f16.cu", "rows_ssln_f32.cu", "rows_bf16.cu"),
-    "group": ("common.cuh", "launch.h", "group_kernels.cuh", "group_norm.cu", "group_f32.cu",
-              "group_f16.cu", "group_bf16.cu"),
+    "group": ("common.cuh", "bulk.cuh", "launch.h", "group_kernels.cuh", "group_norm.cu",
+              "group_f32.cu", "group_f16.cu", "group_bf16.cu"),
 }
 
 

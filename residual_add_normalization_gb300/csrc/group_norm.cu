@@ -130,9 +130,11 @@ static bool allow_smem(void* fn, size_t smem, int dev) {
 
 // Dynamic shared memory of route 2: the phase area up to coop_k_offset, then
 // R[groups] and the second-round R[groups] (padded to 16 bytes), gamma[C]
-// and beta[C].
-static size_t coop_smem_bytes(int PL, int C, int B, int groups) {
-  return (coop_k_offset(PL, C, B, groups) + coop_tail_floats(groups) + 2ull * C) * sizeof(float);
+// and beta[C]; with 16-byte vectors (`slab` > 0) then the slab area
+// (coop_slab_bytes).
+static size_t coop_smem_bytes(int PL, int C, int B, int groups, size_t slab = 0) {
+  return (coop_k_offset(PL, C, B, groups) + coop_tail_floats(groups) + 2ull * C) * sizeof(float) +
+         slab;
 }
 
 GroupPlan two_phase_plan(const SkipGroupCall& c) {
@@ -380,7 +382,13 @@ static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, i
       const int64_t ppc = cdiv(HW, B);
       if (ppc > static_cast<int64_t>(nv) * PL) continue;  // slab too big for nv
       const int64_t Bn = cdiv(HW, ppc);  // CTAs actually needed per item
-      const size_t smem = coop_smem_bytes(PL, static_cast<int>(c.C), static_cast<int>(Bn), c.groups);
+      // 16-byte vectors: the CTA's slab comes in by bulk copies into shared memory
+      const size_t slab = ve * dtype_size(c.t) == 16
+                              ? coop_slab_bytes(static_cast<int>(ppc), static_cast<int>(c.C),
+                                                dtype_size(c.t), c.bcast)
+                              : 0;
+      const size_t smem =
+          coop_smem_bytes(PL, static_cast<int>(c.C), static_cast<int>(Bn), c.groups, slab);
       if (smem > smem_cap) continue;
       if (smem > smem1) {
         int again = 0;

@@ -24,6 +24,7 @@
 // producer issue nothing, so the consumers' waits run out.
 #pragma once
 
+#include "bulk.cuh"
 #include "rows.cuh"
 
 namespace b200norm {
@@ -43,58 +44,6 @@ constexpr size_t kPipeSmemBytes =
     2u * kPipeStages * kPipeTileBytes + 2u * kPipeStages * sizeof(unsigned long long);
 constexpr unsigned long long kPipeLimitNs = 1000000000ull;   // waits for copies / consumers
 constexpr unsigned long long kPipeDrainNs = 1000000000ull;   // the producer's final waits
-
-__device__ __forceinline__ unsigned smem_addr(const void* p) {
-  return static_cast<unsigned>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count)
-               : "memory");
-}
-
-// Makes the initialised barriers visible to the async proxy (the copy engine).
-__device__ __forceinline__ void mbar_init_fence() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, unsigned bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-               :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, unsigned parity) {
-  unsigned done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
-  return done != 0;
-}
-
-// Waits until the phase of parity `parity` has completed; false after limit_ns.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity,
-                                          unsigned long long limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > limit_ns) return false;
-  return true;
-}
-
-// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
-// from global to this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes,
-                                          unsigned long long* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
-}
 
 // Op must provide Elem, P (its 16-byte pack), src0 / src1 (the two streamed
 // inputs, rows * n elements each), load_pair, and the lane kernel's
