@@ -54,8 +54,8 @@ FALLBACK_HBM_GBS = 6800.0
 # captured for the current sources).
 NCU_TRAFFIC = {
     # ncu (dram__bytes_read.sum + dram__bytes_write.sum) of the GatedRMSNorm lane
-    # kernel: 536.9 MB read + 230.2 MB written
-    ("gated_fp16_4x4096x8192_c128", "0f7436073f2436f5"): 767067136,
+    # kernel: 536,953,600 B read + 230,329,856 B written
+    ("gated_fp16_4x4096x8192_c128", "66e3dfe592b810f8"): 767283456,
 }
 
 
