@@ -43,6 +43,9 @@ B200NORM_API b200norm_status b200norm_testing_noalloc_barrier_timeout(uint64_t l
  *                4 = NHWC through L2 (statistics kernel, then apply kernel)
  *                5 = NHWC through L2 in one cooperative grid (statistics, a
  *                    bounded grid barrier, then a second pass over L2)
+ *                6 = NHWC cooperative grid with each CTA's slab of pixels
+ *                    resident in shared memory (bulk copies in and out with
+ *                    16-byte vectors), one bounded grid barrier
  * Other values are rejected with B200NORM_ERR_INVALID_ARGUMENT.  A later
  * SkipGroupNorm call that the forced route cannot take returns
  * B200NORM_ERR_UNSUPPORTED. */

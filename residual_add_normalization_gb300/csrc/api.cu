@@ -438,9 +438,9 @@ b200norm_status b200norm_testing_barrier_timeout(void* workspace, size_t workspa
 }
 
 b200norm_status b200norm_testing_force(int row_mode, int group_route) {
-  if (row_mode < 0 || row_mode > 3 || group_route < 0 || group_route == 1 || group_route > 5)
+  if (row_mode < 0 || row_mode > 3 || group_route < 0 || group_route == 1 || group_route > 6)
     return fail(B200NORM_ERR_INVALID_ARGUMENT,
-                "row_mode in {0, 1, 2, 3}, group_route in {0, 2, 3, 4, 5}");
+                "row_mode in {0, 1, 2, 3}, group_route in {0, 2, 3, 4, 5, 6}");
   g_force_row_mode = row_mode;
   g_force_group_route = group_route;
   return ok();

@@ -16,6 +16,12 @@ void* group_resident_kernel_bf16(DType m, int ve) {
   return nullptr;
 }
 
+void* group_slab_kernel_bf16(DType m, int ve) {
+  if (m == DType::F32) return pick_slab<__nv_bfloat16, float>(ve);
+  if (m == DType::BF16) return pick_slab<__nv_bfloat16, __nv_bfloat16>(ve);
+  return nullptr;
+}
+
 void* group_coop_l2_kernel_bf16(DType m, int ve, bool bcast) {
   if (m == DType::F32) return pick_coop_l2<__nv_bfloat16, float>(ve, bcast);
   if (m == DType::BF16) return pick_coop_l2<__nv_bfloat16, __nv_bfloat16>(ve, bcast);

@@ -16,6 +16,12 @@ void* group_resident_kernel_f16(DType m, int ve) {
   return nullptr;
 }
 
+void* group_slab_kernel_f16(DType m, int ve) {
+  if (m == DType::F32) return pick_slab<__half, float>(ve);
+  if (m == DType::F16) return pick_slab<__half, __half>(ve);
+  return nullptr;
+}
+
 void* group_coop_l2_kernel_f16(DType m, int ve, bool bcast) {
   if (m == DType::F32) return pick_coop_l2<__half, float>(ve, bcast);
   if (m == DType::F16) return pick_coop_l2<__half, __half>(ve, bcast);

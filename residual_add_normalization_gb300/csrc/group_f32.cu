@@ -16,6 +16,12 @@ void* group_resident_kernel_f32(DType m, int ve) {
   return nullptr;
 }
 
+void* group_slab_kernel_f32(DType m, int ve) {
+  if (m == DType::F32) return pick_slab<float, float>(ve);
+  if (m == DType::F16) return pick_slab<float, __half>(ve);
+  return nullptr;
+}
+
 void* group_coop_l2_kernel_f32(DType m, int ve, bool bcast) {
   if (m == DType::F32) return pick_coop_l2<float, float>(ve, bcast);
   if (m == DType::F16) return pick_coop_l2<float, __half>(ve, bcast);

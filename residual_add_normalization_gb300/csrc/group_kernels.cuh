@@ -731,6 +731,275 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
 }
 
 // ---------------------------------------------------------------------------
+// Route 6: NHWC, cooperative grid, the CTA's slab resident in shared memory
+// ---------------------------------------------------------------------------
+// Route 2's pixel ranges, pieces, bounded grid barrier and merge, but the
+// CTA's slab of X -- and its S, formed in place -- lives in shared memory
+// rather than registers, so a slab may hold as many pixels as shared memory
+// takes (route 2: at most eight per thread) and nothing is read twice from
+// HBM or L2.  With 16-byte vectors the slab (and a full-shape skip's) comes
+// in by bulk copies and S goes back out by one bulk store, issued between the
+// CTA's arrival at the grid barrier and its wait; otherwise every thread
+// moves its own vectors.
+// Dynamic shared memory: route 2's pieces / merge area and tail (up to the
+// end of beta), then the copy's mbarrier (16 bytes) | S slab [ppc][C] |
+// (full-shape skip) skip slab [ppc][C].
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from this CTA's shared memory to global memory, as one bulk async-group.
+__device__ __forceinline__ void bulk_store_group(void* dst, const void* src, unsigned bytes) {
+  asm volatile(
+      "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\t"
+      "cp.async.bulk.commit_group;"
+      :: "l"(dst), "r"(smem_addr(src)), "r"(bytes) : "memory");
+}
+
+// Waits until every bulk store of this thread has read its shared memory.
+__device__ __forceinline__ void bulk_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+template <typename T, typename M, int VE>
+__global__ void __launch_bounds__(kCoopMaxThreads, 1)
+sgn_nhwc_slab(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
+  pdl_wait();
+  pdl_trigger();
+  using P = Pack<T, VE>;
+  extern __shared__ float4 smem4[];
+  float* smem = reinterpret_cast<float*>(smem4);
+  float* s_R0 = smem + k_offset;
+  float* s_R = s_R0 + a.groups;
+  __shared__ int s_again;
+  const int C = a.C;
+  const int CV = C / VE;
+  const int PL = blockDim.x / CV;
+  const int tc = threadIdx.x % CV;
+  const int tp = threadIdx.x / CV;
+  const int n = blockIdx.x / B;
+  const int p0 = (blockIdx.x % B) * ppc;
+  const int p1 = min(p0 + ppc, a.HW);
+  const int np = p1 - p0;
+  const int64_t nbase = static_cast<int64_t>(n) * a.HW * C;
+  const int c0 = tc * VE;
+  constexpr bool kBulk = VE * sizeof(T) == 16;
+  float* s_ga = s_R0 + coop_tail_floats(a.groups);  // 16-byte aligned
+  float* s_be = s_ga + C;
+  unsigned long long* s_bar = reinterpret_cast<unsigned long long*>(s_be + C);
+  P* s_S = reinterpret_cast<P*>(s_bar + 2);             // [ppc][CV]: X, then S
+  P* s_K = s_S + static_cast<int64_t>(ppc) * CV;       // [ppc][CV]: full-shape skip
+  const unsigned slab = static_cast<unsigned>(np) * static_cast<unsigned>(C) * sizeof(T);
+
+  // --- the slab into shared memory ------------------------------------------
+  if constexpr (kBulk) {
+    if (threadIdx.x == 0) {
+      mbar_init(s_bar, 1u);
+      mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int64_t at = nbase + static_cast<int64_t>(p0) * C;
+      mbar_arrive_expect_tx(s_bar, a.bcast ? slab : 2u * slab);
+      bulk_load(s_S, a.x + at, slab, s_bar);
+      if (!a.bcast) bulk_load(s_K, a.skip + at, slab, s_bar);
+    }
+  } else {
+    for (int q = tp; q < np; q += PL) {
+      const int64_t off = nbase + static_cast<int64_t>(p0 + q) * C + c0;
+      s_S[q * CV + tc] = ld_stream<T, VE>(a.x + off);
+      if (!a.bcast) s_K[q * CV + tc] = ld_stream<T, VE>(a.skip + off);
+    }
+  }
+  P skb, bv;
+  if (a.bcast) skb = ld_reuse<T, VE>(a.skip + static_cast<int64_t>(n) * C + c0);
+  if (a.bias) bv = ld_reuse<T, VE>(a.bias + c0);
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    s_ga[c] = to_f32(__ldg(a.gamma + c));
+    s_be[c] = to_f32(__ldg(a.beta + c));
+  }
+  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) s_R0[gg] = nhwc_ref(a, n, gg, p0, p1);
+  if (threadIdx.x == 0) s_again = 0;
+  __syncthreads();
+  bool landed = true;
+  if constexpr (kBulk) {
+    // a copy that has not landed within the limit is recorded and the CTA
+    // carries on (its outputs are then undefined) so that the grid barrier
+    // still completes; it waits for the copy again before it leaves
+    landed = mbar_wait(s_bar, 0u, a.limit_ns);
+    if (!landed) {
+      atomicExch(&a.ctl->error, kStatusDeviceTimeout);
+      atomicExch(&a.ctl->error_site, 6u);
+    }
+  }
+
+  // --- S in place, and the sums of S - R and (S - R)^2 ----------------------
+  float Kl[VE], lsum[VE], lsq[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) {
+    Kl[e] = s_R0[fdiv(c0 + e, a.cpg_div)];
+    lsum[e] = lsq[e] = 0.0f;
+  }
+#pragma unroll 2
+  for (int q = tp; q < np; q += PL) {
+    const P xv = s_S[q * CV + tc];
+    P kv;
+    if (!a.bcast) kv = s_K[q * CV + tc];
+    P sv;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) {
+      const float sk = a.bcast ? to_f32(skb.v[e]) : to_f32(kv.v[e]);
+      sv.v[e] = sgn_sum_b<T>(to_f32(xv.v[e]), sk, to_f32(bv.v[e]), a.bias != nullptr);
+      const float d = to_f32(sv.v[e]) - Kl[e];
+      lsum[e] += d;
+      lsq[e] = fmaf(d, d, lsq[e]);
+    }
+    s_S[q * CV + tc] = sv;
+  }
+
+  // --- this CTA's pieces, per group (route 2's combine; a second round
+  // re-reads S from shared memory) --------------------------------------------
+  float* s_acc = smem;
+  float* s_col = smem + 2 * PL * C;
+  const int nthr = PL * CV;
+  const float n_cta = static_cast<float>(np) * static_cast<float>(a.cpg);
+  for (int round = 0; round < 2; ++round) {
+    if (round == 1) {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        Kl[e] = s_R[fdiv(c0 + e, a.cpg_div)];
+        lsum[e] = lsq[e] = 0.0f;
+      }
+      for (int q = tp; q < np; q += PL) {
+        const P sv = s_S[q * CV + tc];
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          const float d = to_f32(sv.v[e]) - Kl[e];
+          lsum[e] += d;
+          lsq[e] = fmaf(d, d, lsq[e]);
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < VE; ++e) {
+      s_acc[(e * PL + tp) * CV + tc] = lsum[e];
+      s_acc[nthr * VE + (e * PL + tp) * CV + tc] = lsq[e];
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < C; j += blockDim.x) {
+      const int e = j / CV, q0 = j % CV;
+      float t1 = 0.0f, t2 = 0.0f;
+      for (int q = 0; q < PL; ++q) {
+        t1 += s_acc[(e * PL + q) * CV + q0];
+        t2 += s_acc[nthr * VE + (e * PL + q) * CV + q0];
+      }
+      s_col[q0 * VE + e] = t1;
+      s_col[C + q0 * VE + e] = t2;
+    }
+    __syncthreads();
+    for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
+      float t1 = 0.0f, t2 = 0.0f;
+      for (int cc = 0; cc < a.cpg; ++cc) {
+        t1 += s_col[gg * a.cpg + cc];
+        t2 += s_col[C + gg * a.cpg + cc];
+      }
+      const float R = round == 0 ? s_R0[gg] : s_R[gg];
+      const float4 piece = piece_from_sums(n_cta, R, t1, t2);
+      a.part[static_cast<int64_t>(blockIdx.x) * a.groups + gg] = piece;
+      if (round == 0) {
+        s_R[gg] = R + piece.z;
+        if (piece_ill(piece)) s_again = 1;
+      }
+    }
+    __syncthreads();
+    if (!s_again) break;
+  }
+  // S out while the other CTAs arrive: with bulk copies one bulk store of the
+  // slab (its writers make their shared-memory writes visible to the copy
+  // engine before the arrival's barrier)
+  if (kBulk && a.s) fence_proxy_async_smem();
+  grid_arrive(a.ctl);
+  if (a.s) {
+    if constexpr (kBulk) {
+      if (threadIdx.x == 0) bulk_store_group(a.s + nbase + static_cast<int64_t>(p0) * C, s_S, slab);
+    } else {
+      for (int q = tp; q < np; q += PL)
+        st_stream<T, VE>(a.s + nbase + static_cast<int64_t>(p0 + q) * C + c0, s_S[q * CV + tc]);
+    }
+  }
+  unsigned departure = 0u;
+  if (!grid_wait(a.ctl, gridDim.x, a.limit_ns, 6u, departure)) {
+    if (kBulk && threadIdx.x == 0) {
+      if (!landed) mbar_wait(s_bar, 0u, a.limit_ns);
+      if (a.s) bulk_store_wait_read();
+    }
+    grid_depart(a.ctl, departure);
+    return;
+  }
+
+  // --- merge the batch item's B pieces per group (route 2's merge) ----------
+  const int nchunk = (B + kCoopMergeChunk - 1) / kCoopMergeChunk;
+  float4* s_cp = reinterpret_cast<float4*>(smem);      // nchunk * groups
+  float* s_gK = smem + nchunk * a.groups * 4;
+  float* s_gd = s_gK + a.groups;
+  float* s_grstd = s_gd + a.groups;
+  const float4* src = a.part + static_cast<int64_t>(n) * B * a.groups;
+  for (int idx = threadIdx.x; idx < nchunk * a.groups; idx += blockDim.x) {
+    const int gg = idx % a.groups, q = idx / a.groups;
+    const int b0 = q * kCoopMergeChunk;
+    float4 u[kCoopMergeChunk];
+#pragma unroll
+    for (int j = 0; j < kCoopMergeChunk; ++j)
+      if (b0 + j < B) u[j] = __ldcg(src + static_cast<int64_t>(b0 + j) * a.groups + gg);
+    const float Kq = piece_mean(u[0]);
+    MergeAcc m{0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int j = 0; j < kCoopMergeChunk; ++j)
+      if (b0 + j < B) merge_add(m, u[j], Kq);
+    s_cp[idx] = make_float4(Kq, m.n, m.s1, m.s2);
+  }
+  __syncthreads();
+  for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) {
+    const float Kc = s_cp[gg].x;
+    MergeAcc m{0.0f, 0.0f, 0.0f};
+    for (int q = 0; q < nchunk; ++q) merge_add_moved(m, s_cp[q * a.groups + gg], Kc);
+    GStats st = merge_finish(m, Kc);
+    if (merge_ill(st))  // pathological spread of the pieces: merge them all afresh
+      st = merge_pieces_global(src, a.groups, gg, B);
+    s_gK[gg] = st.K;
+    s_gd[gg] = st.d;
+    s_grstd[gg] = 1.0f / sqrtf(st.var + a.eps);
+  }
+  __syncthreads();
+  // --- normalize the slab; store Y ------------------------------------------
+  float Kg[VE], mu[VE], rs[VE], ga[VE], be[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) {
+    const unsigned ge = fdiv(c0 + e, a.cpg_div);
+    Kg[e] = s_gK[ge];
+    mu[e] = s_gd[ge];
+    rs[e] = s_grstd[ge];
+  }
+  lds_vec<VE>(s_ga + c0, ga);
+  lds_vec<VE>(s_be + c0, be);
+#pragma unroll 2
+  for (int q = tp; q < np; q += PL) {
+    const P sv = s_S[q * CV + tc];
+    P out;
+#pragma unroll
+    for (int e = 0; e < VE; ++e)
+      out.v[e] = from_f32<T>(sgn_out(to_f32(sv.v[e]), Kg[e], mu[e], rs[e], ga[e], be[e], a.act));
+    st_stream<T, VE>(a.y + nbase + static_cast<int64_t>(p0 + q) * C + c0, out);
+  }
+  if (kBulk && threadIdx.x == 0) {
+    if (!landed) mbar_wait(s_bar, 0u, a.limit_ns);
+    if (a.s) bulk_store_wait_read();  // the S store has read the slab
+  }
+  grid_depart(a.ctl, departure);
+}
+
+// ---------------------------------------------------------------------------
 // Route 4: NHWC through L2, two kernels
 // ---------------------------------------------------------------------------
 // For NHWC tensors small enough to stay in L2 between two kernels.  Both
@@ -1319,6 +1588,13 @@ inline void* pick_coop(int ve, int nv) {
 }
 
 template <typename T, typename M>
+inline void* pick_slab(int ve) {
+  constexpr int V16 = static_cast<int>(16 / sizeof(T));
+  return ve == 1 ? reinterpret_cast<void*>(sgn_nhwc_slab<T, M, 1>)
+                 : reinterpret_cast<void*>(sgn_nhwc_slab<T, M, V16>);
+}
+
+template <typename T, typename M>
 inline void* pick_resident(int ve) {
   constexpr int V16 = static_cast<int>(16 / sizeof(T));
   return ve == 1 ? reinterpret_cast<void*>(sgn_nchw_smem<T, M, 1>)
@@ -1418,6 +1694,19 @@ inline cudaError_t launch_group_typed(const SkipGroupCall& c, const GroupPlan& p
     void* args[] = {&a, &B, &ppc, &koff};
     return cudaLaunchKernelExC(&cfg, fn, args);
   }
+  if (p.route == 6) {
+    // A cooperative launch keeps plain stream order (no early scheduling).
+    void* fn = pick_slab<T, M>(p.ve);
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int B = p.ctas_per_item, ppc = p.pix_per_cta;
+    const int PL = p.block / static_cast<int>(c.C / p.ve);
+    int koff = static_cast<int>(coop_k_offset(PL, static_cast<int>(c.C), B, c.groups));
+    void* args[] = {&a, &B, &ppc, &koff};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+  }
   if (p.route == 5) {
     // A cooperative launch keeps plain stream order (no early scheduling).
     void* fn = pick_coop_l2<T, M>(p.ve, c.bcast);
@@ -1465,6 +1754,9 @@ void* group_coop_kernel_bf16(DType m, int ve, int nv);
 void* group_resident_kernel_f32(DType m, int ve);
 void* group_resident_kernel_f16(DType m, int ve);
 void* group_resident_kernel_bf16(DType m, int ve);
+void* group_slab_kernel_f32(DType m, int ve);
+void* group_slab_kernel_f16(DType m, int ve);
+void* group_slab_kernel_bf16(DType m, int ve);
 void* group_coop_l2_kernel_f32(DType m, int ve, bool bcast);
 void* group_coop_l2_kernel_f16(DType m, int ve, bool bcast);
 void* group_coop_l2_kernel_bf16(DType m, int ve, bool bcast);

@@ -81,6 +81,15 @@ static void* pick_coop_l2_any(DType t, DType m, int ve, bool bcast) {
   return nullptr;
 }
 
+static void* pick_slab_any(DType t, DType m, int ve) {
+  switch (t) {
+    case DType::F32: return group_slab_kernel_f32(m, ve);
+    case DType::F16: return group_slab_kernel_f16(m, ve);
+    case DType::BF16: return group_slab_kernel_bf16(m, ve);
+  }
+  return nullptr;
+}
+
 static bool resident_cluster_fits(void* fn, int block, int csize, size_t smem) {
   if (csize > 8 &&
       cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
@@ -232,6 +241,60 @@ static bool plan_coop_l2_route(const SkipGroupCall& c, bool vector_ok, GroupPlan
   return true;
 }
 
+// Route 6: route 2 with the slab resident in shared memory.  One CTA per SM
+// share of the batch items (at least one CTA per item), as long as the slab
+// of X (and of a full-shape skip) fits next to route 2's other shared memory
+// and every CTA can be resident at once.
+static bool plan_slab_route(const SkipGroupCall& c, bool vector_ok, GroupPlan* p) {
+  if (!c.channels_last) return false;
+  const int64_t es = static_cast<int64_t>(dtype_size(c.t));
+  const int vec = static_cast<int>(16 / es);
+  const int ve = (vector_ok && c.C % vec == 0) ? vec : 1;
+  const int64_t CV = c.C / ve;
+  const int64_t HW = c.H * c.W;
+  if (CV > kCoopMaxThreads || HW > 0x7fffffffLL) return false;
+  int dev = 0, sms = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  void* fn = pick_slab_any(c.t, c.m, ve);
+  cudaFuncAttributes fa;
+  if (!fn || cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  const size_t cap = static_cast<size_t>(optin) - fa.sharedSizeBytes;
+  const int PL = static_cast<int>(kCoopMaxThreads / CV);
+  const int block = static_cast<int>(PL * CV);
+  int64_t B = std::max<int64_t>(1, sms / c.N);
+  const int64_t ppc = cdiv(HW, B);
+  B = cdiv(HW, ppc);
+  if (B * c.N > kMaxCoopCtas || ppc * c.C > 0x7fffffffLL) return false;
+  const size_t slab = 16 + static_cast<size_t>(ppc) * c.C * es * (c.bcast ? 1 : 2);
+  const size_t smem = coop_smem_bytes(PL, static_cast<int>(c.C), static_cast<int>(B), c.groups, slab);
+  int per_sm = 0;
+  if (smem > cap || !allow_smem(fn, smem, dev) ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, block, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (static_cast<int64_t>(per_sm) * sms < B * c.N) return false;
+  *p = GroupPlan{};
+  p->route = 6;
+  p->ve = ve;
+  p->nv = static_cast<int>(cdiv(ppc, PL));
+  p->block = block;
+  p->csize = 1;
+  p->grid = B * c.N;
+  p->ctas_per_item = static_cast<int>(B);
+  p->pix_per_cta = static_cast<int>(ppc);
+  p->smem = smem;
+  return true;
+}
+
 static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, int force,
                                        GroupPlan* p);
 
@@ -281,14 +344,19 @@ static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, i
   }
   if (force == 4) return plan_l2_route(c, vector_ok, p) ? cudaSuccess : cudaErrorNotSupported;
   if (force == 5) return plan_coop_l2_route(c, vector_ok, p) ? cudaSuccess : cudaErrorNotSupported;
+  if (force == 6) return plan_slab_route(c, vector_ok, p) ? cudaSuccess : cudaErrorNotSupported;
   if (force == 0 && c.channels_last) {
     // NHWC: the cooperative route whenever its grid can hold the pixels in
-    // registers, else one cooperative grid re-reading through L2, else the
-    // two-kernel L2 route, else two-phase.  (Measured on GB300: (2, 64, 64,
-    // 320) fp16 9.9 us cooperative vs 13.3 / 13.5 us through L2 in one grid /
-    // two kernels; (4, 64, 64, 320) fp16 16.8 vs 17.5 us and fp32 (2, 64, 64,
-    // 320) 13.9 vs 15.2 us through L2 in one grid vs two kernels.)
+    // registers, else the cooperative route with the slabs in shared memory,
+    // else one cooperative grid re-reading through L2, else the two-kernel
+    // L2 route, else two-phase.  (Measured on GB300, graph-timed: (2, 64,
+    // 64, 320) fp16 9.3 us in registers vs 10.6 in shared memory and 13.3 /
+    // 13.5 through L2 in one grid / two kernels; slabs in shared memory
+    // against one grid through L2: (4, 64, 64, 320) fp16 13.7 vs 16.5 us,
+    // (2, 64, 64, 640) fp16 14.2 vs 18.3, (2, 64, 64, 320) fp32 11.3 vs
+    // 14.8, (8, 64, 64, 320) fp16 20.4 vs 22.8.)
     if (plan_group_uncached(c, vector_ok, 2, p) == cudaSuccess) return cudaSuccess;
+    if (plan_slab_route(c, vector_ok, p)) return cudaSuccess;
     if (plan_coop_l2_route(c, vector_ok, p)) return cudaSuccess;
     if (plan_l2_route(c, vector_ok, p)) return cudaSuccess;
     *p = two_phase_plan(c);

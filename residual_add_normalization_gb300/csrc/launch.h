@@ -160,6 +160,7 @@ struct GroupPlan {
                   // 3: two-phase partials -> normalize (any shape)
                   // 4: NHWC through L2 (statistics kernel, then apply kernel)
                   // 5: NHWC through L2 in one cooperative grid (grid barrier)
+                  // 6: NHWC cooperative, slab resident in shared memory
   int ve;         // elements per vector access, or 1
   int nv;         // vectors held per thread
   int block;      // threads per CTA

@@ -241,7 +241,8 @@ def test_force_hook_validation(lib):
     assert lib.b200norm_testing_force(-1, 0) == INVALID
     assert lib.b200norm_testing_force(1, 0) == OK
     assert lib.b200norm_testing_force(0, 1) == INVALID
-    assert lib.b200norm_testing_force(0, 6) == INVALID
+    assert lib.b200norm_testing_force(0, 6) == OK
+    assert lib.b200norm_testing_force(0, 7) == INVALID
     assert lib.b200norm_testing_force(0, 5) == OK
     assert lib.b200norm_testing_force(0, 0) == OK
     assert lib.b200norm_testing_force(4, 0) == INVALID

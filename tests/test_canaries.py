@@ -98,6 +98,9 @@ GROUP_CASES = [  # (shape, channels_last, groups, skip, forced route, shift)
     ((2, 64, 16, 16), 0, 8, "full", 3, 0),        # route 3, NCHW
     ((4, 32, 32, 320), 1, 32, "nc", 4, 0),        # route 4
     ((4, 32, 32, 320), 1, 32, "nc", 5, 0),        # route 5
+    ((4, 32, 32, 320), 1, 32, "full", 6, 0),      # route 6 (slab in shared memory, bulk copies)
+    ((1, 33, 17, 40), 1, 8, "nc", 6, 0),          # route 6, ragged last slab
+    ((3, 5, 7, 12), 1, 3, "full", 6, 1),          # route 6, scalar path, unaligned outputs
     ((3, 5, 7, 12), 1, 3, "nc", 0, 1),            # scalar path, unaligned outputs
 ]
 

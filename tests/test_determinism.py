@@ -62,6 +62,7 @@ def test_gated_repeatable(row_mode):
     ((2, 64, 64, 320), 1, 0),   # cooperative grid (route 2)
     ((4, 64, 64, 320), 1, 4),   # through L2, two kernels (route 4)
     ((4, 64, 64, 320), 1, 5),   # through L2, one cooperative grid (route 5)
+    ((4, 64, 64, 320), 1, 6),   # slab in shared memory, one cooperative grid (route 6)
     ((2, 32, 32, 320), 1, 3),   # two-phase
     ((16, 1280, 16, 16), 0, 0), # NCHW resident
     ((1, 320, 64, 64), 0, 0),   # NCHW clusters

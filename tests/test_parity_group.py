@@ -1,9 +1,10 @@
 """GPU parity: SkipGroupNorm kernels against the CPU oracle on the same seeded
 inputs, through the C ABI (via the binding).
 
-Covers the four routes (NCHW: CTA / cluster per group instance; NHWC: a
-statistics kernel and an apply kernel through L2, or a cooperative grid with
-one bounded grid barrier; two-phase for anything else),
+Covers the six routes (NCHW: CTA / cluster per group instance; NHWC: a
+cooperative grid with one bounded grid barrier holding its slabs in
+registers or in shared memory, one cooperative grid or a statistics kernel
+and an apply kernel through L2; two-phase for anything else),
 both layouts, both T and both M, full / (N, C) / (N, 1, 1, C) skip, bias and S
 on and off, SiLU on and off, vector and scalar paths, and ragged slabs.
 """
@@ -129,13 +130,14 @@ def test_forced_two_phase(cl, dtype):
     check(d, 8, 1, cl)
 
 
-@pytest.mark.parametrize("route", [2, 4, 5])
+@pytest.mark.parametrize("route", [2, 4, 5, 6])
 @pytest.mark.parametrize("dtype,mdtype", TYPE_PAIRS)
 @pytest.mark.parametrize("case", NHWC_CASES)
 def test_nhwc_forced_routes(route, dtype, mdtype, case):
-    """The NHWC routes 2, 4 and 5 on every NHWC case each can take (route 2
-    holds a resident grid's pixels in registers; routes 4 and 5 re-read
-    tensors that stay in L2, in two launches or in one cooperative grid)."""
+    """The NHWC routes 2, 4, 5 and 6 on every NHWC case each can take (route
+    2 holds a resident grid's pixels in registers, route 6 in shared memory;
+    routes 4 and 5 re-read tensors that stay in L2, in two launches or in one
+    cooperative grid)."""
     N, H, W, C, G = case
     assert b2.library().b200norm_testing_force(0, route) == 0
     for skip, bias, act, want_sum in (("nc", True, 1, True), ("full", False, 0, False)):
@@ -156,14 +158,16 @@ def test_route_coverage():
         routes.add((p["route"], p["csize"] > 1))
     for N, H, W, C, G in NHWC_CASES:
         routes.add((plan((N, H, W, C), G, np.float16, np.float32, 1)["route"], False))
-    assert {1, 2, 3} <= {r for r, _ in routes} <= {1, 2, 3, 5}
+    assert {1, 2, 3} <= {r for r, _ in routes} <= {1, 2, 3, 5, 6}
     assert (1, True) in routes, "no cluster-per-instance case"
     # the cooperative route while its grid can hold the pixels in registers,
-    # else one cooperative grid through L2 (also for more batch items than the
-    # two-kernel L2 route counts)
+    # else the cooperative route with the slabs in shared memory, else one
+    # cooperative grid through L2.  (The plan query assumes a full-shape skip,
+    # whose slab in shared memory doubles that of X.)
     assert plan((2, 64, 64, 320), 32, np.float16, np.float32, 1)["route"] == 2
     assert plan((64, 8, 8, 64), 8, np.float16, np.float32, 1)["route"] == 2
-    assert plan((4, 64, 64, 320), 32, np.float16, np.float32, 1)["route"] == 5
+    assert plan((4, 64, 64, 320), 32, np.float16, np.float32, 1)["route"] == 6
+    assert plan((16, 32, 32, 320), 32, np.float16, np.float32, 1)["route"] == 6
     assert plan((2, 128, 128, 320), 32, np.float16, np.float32, 1)["route"] == 5
     assert plan((64, 24, 24, 320), 32, np.float16, np.float32, 1)["route"] == 5
 

@@ -13,7 +13,7 @@ to: each group's first element (positive and negative), each group's first
 element and quarter points, and three random elements of each group.
 Routes: NCHW one CTA per instance (10,240-element groups), clusters per
 instance (10,240- and 40,960-element groups) and the forced two-phase route;
-NHWC the automatic (cooperative) route and the forced routes 3, 4 and 5.
+NHWC the automatic (cooperative) route and the forced routes 3, 4, 5 and 6.
 """
 import numpy as np
 import pytest
@@ -102,7 +102,7 @@ def test_nchw_outliers(shape, groups, force, dtype, mdtype, pattern, A):
 
 @pytest.mark.parametrize("pattern,A", PATTERNS)
 @pytest.mark.parametrize("dtype,mdtype", TYPES)
-@pytest.mark.parametrize("route", [0, 3, 4, 5])
+@pytest.mark.parametrize("route", [0, 3, 4, 5, 6])
 def test_nhwc_outliers(route, dtype, mdtype, pattern, A):
     shape, groups = (2, 64, 64, 320), 32
     d = synthetic.skip_group_inputs(shape, dtype, mdtype, seed=22, channels_last=1, skip="nc",
@@ -112,10 +112,10 @@ def test_nhwc_outliers(route, dtype, mdtype, pattern, A):
     run_check(d, groups, 1, 1)
 
 
-@pytest.mark.parametrize("route", [0, 3, 4, 5])
+@pytest.mark.parametrize("route", [0, 3, 4, 5, 6])
 @pytest.mark.parametrize("cl", [0, 1])
 def test_bf16_outliers(cl, route):
-    if not cl and route in (4, 5):
+    if not cl and route in (4, 5, 6):
         pytest.skip("NHWC-only route")
     shape = (2, 64, 64, 320) if cl else (2, 1280, 16, 16)
     d = synthetic.skip_group_inputs(shape, BF16, np.float32, seed=23, channels_last=cl,
