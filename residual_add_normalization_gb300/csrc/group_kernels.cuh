@@ -442,17 +442,15 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
 //            offset d[groups] | rstd[groups]
 //   tail at k_offset, kept throughout: R[groups] | second-round R[groups]
 //            (padded to 16 bytes) | gamma[C] | beta[C]
-//   then, with 16-byte vectors: the copy's mbarrier (16 bytes) | the CTA's
-//            slab of X | (full-shape skip) its slab of skip
-// With 16-byte vectors every pixel is a whole number of 16-byte vectors, so
-// the CTA's slab -- pixels [p0, p1) of its batch item, one contiguous run --
-// comes in by one bulk copy into shared memory (a second one for a full-shape
-// skip) instead of NV loads per thread; each thread then takes its vectors
-// from there.  (Measured on the NHWC fp16 workload: 9.2 us per call against
-// 9.85 with the per-thread loads.)
+// Each thread loads its own NV vectors of X (and skip) with streaming 16-byte
+// loads, all issued before the first is used.  (A bulk copy of the CTA's slab
+// into shared memory, which route 6 uses, was slower here with the inputs in
+// HBM: 10.1 against 9.9 us per call on the NHWC fp16 workload, and no faster
+// when issued earlier or split into 4 or 8 copies; it wins only when the
+// inputs are already in L2.)
 constexpr int kCoopMergeChunk = 8;
 
-// Bytes of route 2's slab area: the mbarrier, then the X slab and (full skip)
+// Bytes of route 6's slab area: the mbarrier, then the S slab and (full skip)
 // the skip slab of ppc pixels of C elements of `es` bytes.
 __host__ __device__ constexpr size_t coop_slab_bytes(int ppc, int C, size_t es, bool bcast) {
   return 16 + static_cast<size_t>(ppc) * C * es * (bcast ? 1 : 2);
@@ -501,35 +499,14 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
   const int c0 = tc * VE;
 
   // --- load and form S (stored while the grid barrier is pending) ----------
-  constexpr bool kBulk = VE * sizeof(T) == 16;
-  unsigned long long* s_bar = reinterpret_cast<unsigned long long*>(
-      smem + k_offset + coop_tail_floats(a.groups) + 2 * C);
-  T* s_xs = reinterpret_cast<T*>(s_bar + 2);                          // X slab
-  T* s_ks = s_xs + static_cast<int64_t>(ppc) * C;                    // skip slab
-  const unsigned slab = static_cast<unsigned>((p1 - p0) * C * sizeof(T));
-  if constexpr (kBulk) {
-    if (threadIdx.x == 0) {
-      mbar_init(s_bar, 1u);
-      mbar_init_fence();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const int64_t at = nbase + static_cast<int64_t>(p0) * C;
-      mbar_arrive_expect_tx(s_bar, a.bcast ? slab : 2u * slab);
-      bulk_load(s_xs, a.x + at, slab, s_bar);
-      if (!a.bcast) bulk_load(s_ks, a.skip + at, slab, s_bar);
-    }
-  }
   Pack<T, VE> xv[NV], kv[NV], sv[NV];
-  if constexpr (!kBulk) {
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      const int p = p0 + tp + k * PL;
-      if (p < p1) {
-        const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
-        xv[k] = ld_stream<T, VE>(a.x + off);
-        if (!a.bcast) kv[k] = ld_stream<T, VE>(a.skip + off);
-      }
+  for (int k = 0; k < NV; ++k) {
+    const int p = p0 + tp + k * PL;
+    if (p < p1) {
+      const int64_t off = nbase + static_cast<int64_t>(p) * C + c0;
+      xv[k] = ld_stream<T, VE>(a.x + off);
+      if (!a.bcast) kv[k] = ld_stream<T, VE>(a.skip + off);
     }
   }
   Pack<T, VE> skb, bv;
@@ -545,26 +522,6 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
   for (int gg = threadIdx.x; gg < a.groups; gg += blockDim.x) s_R0[gg] = nhwc_ref(a, n, gg, p0, p1);
   if (threadIdx.x == 0) s_again = 0;
   __syncthreads();
-  bool landed = true;
-  if constexpr (kBulk) {
-    // a copy that has not landed within the limit is recorded and the CTA
-    // carries on (its outputs are then undefined) so that the grid barrier
-    // still completes; it waits for the copy again before it leaves
-    landed = mbar_wait(s_bar, 0u, a.limit_ns);
-    if (!landed) {
-      atomicExch(&a.ctl->error, kStatusDeviceTimeout);
-      atomicExch(&a.ctl->error_site, 2u);
-    }
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      const int p = p0 + tp + k * PL;
-      if (p < p1) {
-        const int64_t off = static_cast<int64_t>(p - p0) * C + c0;
-        xv[k] = *reinterpret_cast<const Pack<T, VE>*>(s_xs + off);
-        if (!a.bcast) kv[k] = *reinterpret_cast<const Pack<T, VE>*>(s_ks + off);
-      }
-    }
-  }
   float Kl[VE];
 #pragma unroll
   for (int e = 0; e < VE; ++e) Kl[e] = s_R0[fdiv(c0 + e, a.cpg_div)];
@@ -658,7 +615,6 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
   }
   unsigned departure = 0u;
   if (!grid_wait(a.ctl, gridDim.x, a.limit_ns, 1u, departure)) {
-    if (kBulk && !landed && threadIdx.x == 0) mbar_wait(s_bar, 0u, a.limit_ns);
     grid_depart(a.ctl, departure);
     return;
   }
@@ -726,7 +682,6 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
       st_stream<T, VE>(a.y + off, out);
     }
   }
-  if (kBulk && !landed && threadIdx.x == 0) mbar_wait(s_bar, 0u, a.limit_ns);
   grid_depart(a.ctl, departure);
 }
 

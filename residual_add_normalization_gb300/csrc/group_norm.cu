@@ -139,8 +139,7 @@ static bool allow_smem(void* fn, size_t smem, int dev) {
 
 // Dynamic shared memory of route 2: the phase area up to coop_k_offset, then
 // R[groups] and the second-round R[groups] (padded to 16 bytes), gamma[C]
-// and beta[C]; with 16-byte vectors (`slab` > 0) then the slab area
-// (coop_slab_bytes).
+// and beta[C]; for route 6 (`slab` > 0) then its slab area (coop_slab_bytes).
 static size_t coop_smem_bytes(int PL, int C, int B, int groups, size_t slab = 0) {
   return (coop_k_offset(PL, C, B, groups) + coop_tail_floats(groups) + 2ull * C) * sizeof(float) +
          slab;
@@ -273,7 +272,7 @@ static bool plan_slab_route(const SkipGroupCall& c, bool vector_ok, GroupPlan* p
   const int64_t ppc = cdiv(HW, B);
   B = cdiv(HW, ppc);
   if (B * c.N > kMaxCoopCtas || ppc * c.C > 0x7fffffffLL) return false;
-  const size_t slab = 16 + static_cast<size_t>(ppc) * c.C * es * (c.bcast ? 1 : 2);
+  const size_t slab = coop_slab_bytes(static_cast<int>(ppc), static_cast<int>(c.C), es, c.bcast);
   const size_t smem = coop_smem_bytes(PL, static_cast<int>(c.C), static_cast<int>(B), c.groups, slab);
   int per_sm = 0;
   if (smem > cap || !allow_smem(fn, smem, dev) ||
@@ -349,9 +348,10 @@ static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, i
     // NHWC: the cooperative route whenever its grid can hold the pixels in
     // registers, else the cooperative route with the slabs in shared memory,
     // else one cooperative grid re-reading through L2, else the two-kernel
-    // L2 route, else two-phase.  (Measured on GB300, graph-timed: (2, 64,
-    // 64, 320) fp16 9.3 us in registers vs 10.6 in shared memory and 13.3 /
-    // 13.5 through L2 in one grid / two kernels; slabs in shared memory
+    // L2 route, else two-phase.  (Measured on GB300, graph-timed with the
+    // inputs in HBM: (2, 64, 64, 320) fp16 9.9 us in registers vs 10.6 in
+    // shared memory and 13.3 / 13.5 through L2 in one grid / two kernels;
+    // slabs in shared memory
     // against one grid through L2: (4, 64, 64, 320) fp16 13.7 vs 16.5 us,
     // (2, 64, 64, 640) fp16 14.2 vs 18.3, (2, 64, 64, 320) fp32 11.3 vs
     // 14.8, (8, 64, 64, 320) fp16 20.4 vs 22.8.)
@@ -450,13 +450,7 @@ static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, i
       const int64_t ppc = cdiv(HW, B);
       if (ppc > static_cast<int64_t>(nv) * PL) continue;  // slab too big for nv
       const int64_t Bn = cdiv(HW, ppc);  // CTAs actually needed per item
-      // 16-byte vectors: the CTA's slab comes in by bulk copies into shared memory
-      const size_t slab = ve * dtype_size(c.t) == 16
-                              ? coop_slab_bytes(static_cast<int>(ppc), static_cast<int>(c.C),
-                                                dtype_size(c.t), c.bcast)
-                              : 0;
-      const size_t smem =
-          coop_smem_bytes(PL, static_cast<int>(c.C), static_cast<int>(Bn), c.groups, slab);
+      const size_t smem = coop_smem_bytes(PL, static_cast<int>(c.C), static_cast<int>(Bn), c.groups);
       if (smem > smem_cap) continue;
       if (smem > smem1) {
         int again = 0;
