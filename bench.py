@@ -44,6 +44,8 @@ BF16_WORKLOADS = ["ssln_bf16_8x2048x4096", "gated_bf16_4x4096x8192_c128",
                   "sgn_nhwc_bf16_2x64x64x320", "sgn_nchw_bf16_16x1280x16x16"]
 # short SkipSimplifiedLayerNormalization rows: the pipelined bulk-copy schedule
 SHORT_WORKLOADS = ["ssln_fp32_262144x128"]
+# mid-size NHWC SkipGroupNorm: the cooperative route with slabs in shared memory
+MID_WORKLOADS = ["sgn_nhwc_fp16_4x64x64x320"]
 # the small SkipSimplifiedLayerNormalization batch: latency-bound, timed on its own
 SMALL_WORKLOADS = ["ssln_fp32_64x768"]
 NOMINAL_HBM_GBS = 8000.0
@@ -373,20 +375,26 @@ def run_ours(args, rank, world, dist):
         del graphs, bcalls
         torch.cuda.synchronize()
 
-    # --- short rows (the pipelined schedule), timed the same way -------------
-    short_ops = {}
-    if not args.no_short:
-        scalls = make_calls(torch, b2, dev, SHORT_WORKLOADS)
+    # --- short rows (the pipelined schedule) and mid-size NHWC SkipGroupNorm
+    # (slabs in shared memory), timed the same way -------------------------------
+    def timed_section(names):
+        scalls = make_calls(torch, b2, dev, names)
         for c in scalls:
             for f in c["fns"]:
                 f()
         torch.cuda.synchronize()
         graphs, sreps = op_graphs_of(torch, scalls, cap)
         sms_ = time_op_graphs(torch, graphs, sreps, stream)
-        short_ops = {c["name"]: op_entry(c, ms) for c, ms in zip(scalls, sms_)}
+        out = {c["name"]: op_entry(c, ms) for c, ms in zip(scalls, sms_)}
         del graphs, scalls
         torch.cuda.synchronize()
+        return out
+
+    short_ops = {}
+    if not args.no_short:
+        short_ops = timed_section(SHORT_WORKLOADS)
         b2.rows_status()
+    mid_ops = {} if args.no_mid else timed_section(MID_WORKLOADS)
 
     # --- latency-bound calls: per-call time in a graph of back-to-back calls -
     def latency_section(names):
@@ -522,6 +530,10 @@ def run_ours(args, rank, world, dist):
         "per_op_short_rows": ({"timing": "as per_op; short rows, which take the pipelined "
                                           "bulk-copy schedule; not part of `value`",
                                **short_ops} if short_ops else None),
+        "per_op_nhwc_mid": ({"timing": "as per_op; NHWC SkipGroupNorm with more pixels than "
+                                       "the cooperative grid holds in registers (slabs in "
+                                       "shared memory, bulk copies); not part of `value`",
+                             **mid_ops} if mid_ops else None),
         "decode": ({"timing": f"best and median of {OP_MIN_ROUNDS} replays of a CUDA graph of "
                               "200 back-to-back calls on one buffer set (inputs L2-resident, as "
                               "when a preceding kernel has just written them); not part of "
@@ -674,13 +686,15 @@ def main():
                     help="skip the decode-shaped latency measurements")
     ap.add_argument("--no-short", action="store_true",
                     help="skip the short-row (pipelined schedule) measurement")
+    ap.add_argument("--no-mid", action="store_true",
+                    help="skip the mid-size NHWC SkipGroupNorm measurement")
     ap.add_argument("--only", choices=STEP_WORKLOADS + BF16_WORKLOADS + DECODE_WORKLOADS +
-                    SHORT_WORKLOADS,
+                    SHORT_WORKLOADS + MID_WORKLOADS,
                     help="run a single workload (for profiler runs; not a bench line)")
     args = ap.parse_args()
     if args.only:
         STEP_WORKLOADS[:] = [args.only]
-        args.no_bf16 = args.no_decode = args.no_short = True
+        args.no_bf16 = args.no_decode = args.no_short = args.no_mid = True
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -114,6 +114,12 @@ WORKLOADS = {
     "ssln_fp32_262144x128": dict(
         op="skip_rms", seed=12, dtype=np.float32, shape=(262144, 128), bias=True,
         gamma=("normal", 1.0, 0.1), epsilon=SSLN_EPS, want_sum=True),
+    # The NHWC fp16 workload at batch 4: more pixels than the cooperative
+    # grid holds in registers, so the slabs stay in shared memory.
+    "sgn_nhwc_fp16_4x64x64x320": dict(
+        op="skip_group", seed=13, dtype=np.float16, mdtype=np.float32,
+        shape=(4, 64, 64, 320), channels_last=1, skip="nc", bias=True, x_std=1.0,
+        groups=32, epsilon=1e-5, activation=1, want_sum=True),
 }
 
 # Order the workloads are listed in (small SSLN first, decode shapes last).
