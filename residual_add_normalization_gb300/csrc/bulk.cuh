@@ -1,7 +1,7 @@
 // bulk.cuh -- bulk asynchronous copies between global and shared memory
 // (sm_103a): mbarrier set-up and bounded waits, and cp.async.bulk loads that
-// complete on an mbarrier.  Used by the pipelined row schedule and the NHWC
-// cooperative SkipGroupNorm route.
+// complete on an mbarrier.  Used by the pipelined row schedule and by the
+// SkipGroupNorm route whose NHWC slabs stay in shared memory (route 6).
 #pragma once
 
 #include "common.cuh"

@@ -5,7 +5,7 @@
 // S = round_T((X + skip) + bias); Y = round_T(act((S - mean) * rstd * gamma[c] + beta[c]))
 // with mean / population variance per (batch item n, group g) over the C/groups
 // channels of g and every spatial position (com.microsoft.SkipGroupNorm README,
-// Description).  Five routes:
+// Description).  Six routes:
 //
 //   1. NCHW resident.  A group instance (n, g) is one contiguous run of
 //      cpg * H * W elements.  One CTA -- or a cluster of up to 16 CTAs for
@@ -26,6 +26,10 @@
 //      by the last CTA of each batch item; then an apply kernel that re-forms
 //      S from inputs still in L2.
 //   5. Route 4's two passes in one cooperative grid with one grid barrier.
+//   6. Route 2 with each CTA's slab in shared memory instead of registers,
+//      for slabs larger than registers hold: bulk copies bring X (and a
+//      full-shape skip) in, S is formed in place and one bulk store sends it
+//      out while the grid barrier is pending.
 //
 // Statistics.  Every piece of a group instance that one CTA (or one cluster
 // rank, or one chunk) sees is summarised as (n, R, mu, m2): n elements, a
