@@ -412,7 +412,7 @@ sgn_nchw_smem(const SgnArgs<T, M> a, int span, FastDiv vpc) {
   } else {
     st = piece_stats(piece);
   }
-  const float rstd = 1.0f / sqrtf(st.var + a.eps);
+  const float rstd = rsqrtf(st.var + a.eps);
   for (int i = threadIdx.x; i < cnt; i += kNchwThreads) {
     const int c = cbase + static_cast<int>(fdiv(static_cast<unsigned>(v0 + i), vpc));
     const float2 gbc = s_gb[c - c_lo];
@@ -658,7 +658,7 @@ sgn_nhwc_coop(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
       st = merge_pieces_global(src, a.groups, gg, B);
     s_gK[gg] = st.K;
     s_gd[gg] = st.d;
-    s_grstd[gg] = 1.0f / sqrtf(st.var + a.eps);
+    s_grstd[gg] = rsqrtf(st.var + a.eps);
   }
   __syncthreads();
   // --- normalize what this thread holds; store Y ---------------------------
@@ -928,7 +928,7 @@ sgn_nhwc_slab(const SgnArgs<T, M> a, int B, int ppc, int k_offset) {
       st = merge_pieces_global(src, a.groups, gg, B);
     s_gK[gg] = st.K;
     s_gd[gg] = st.d;
-    s_grstd[gg] = 1.0f / sqrtf(st.var + a.eps);
+    s_grstd[gg] = rsqrtf(st.var + a.eps);
   }
   __syncthreads();
   // --- normalize the slab; store Y ------------------------------------------
@@ -1152,7 +1152,7 @@ __device__ __forceinline__ void nhwc_merge(const SgnArgs<T, M>& a, const float4*
       st = merge_pieces_global(part, a.groups, g, B);
     s_out[g] = st.K;
     s_out[a.groups + g] = st.d;
-    s_out[2 * a.groups + g] = 1.0f / sqrtf(st.var + a.eps);
+    s_out[2 * a.groups + g] = rsqrtf(st.var + a.eps);
   }
   __syncthreads();
 }
@@ -1485,7 +1485,7 @@ sgn_normalize(const SgnArgs<T, M> a, int chunks) {
     if (!merge_ill(st)) break;  // uniform: every thread holds the same totals
     Kc = Kc + st.d;
   }
-  const float rstd = 1.0f / sqrtf(st.var + a.eps);
+  const float rstd = rsqrtf(st.var + a.eps);
   const int64_t j0 = static_cast<int64_t>(q) * kTwoPhaseChunk;
 #pragma unroll 4
   for (int i = 0; i < kTwoPhaseEpt; ++i) {
