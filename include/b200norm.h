@@ -197,7 +197,8 @@ B200NORM_API b200norm_status b200norm_rows_status(b200norm_stream_t stream);
  *             next call.  Calls that share a workspace must not overlap on the
  *             device (enqueue them on one stream).
  *
- * Cross-CTA waits inside the kernels are bounded: a wait that does not
+ * Device-side waits inside the kernels (on other CTAs at a grid barrier, or
+ * on a bulk copy into shared memory) are bounded: a wait that does not
  * complete within about one second makes the kernel record
  * B200NORM_ERR_DEVICE_TIMEOUT in the workspace and return early (outputs are
  * then undefined).  b200norm_workspace_status() reads that record.
