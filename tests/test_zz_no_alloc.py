@@ -73,13 +73,19 @@ def _call_regular(d, groups, act, cl, want_sum, eps=1e-5):
     return to_host(y), to_host(s)
 
 
-# The NHWC case uses the cooperative route (grid barrier and piece slots in
-# the scratch); the NCHW cases cover the resident route (no slots), the
-# two-phase route (piece slots) and 64 groups (the workspace size of NCHW
-# shapes counts only the two-phase slots).
+# The NHWC cases use the cooperative routes (grid barrier and piece slots in
+# the scratch): slabs in registers (route 2), slabs in shared memory with bulk
+# copies (route 6) and one grid re-reading through L2 (route 5); the NCHW
+# cases cover the resident route (no slots), the two-phase route (piece
+# slots) and 64 groups (the workspace size of NCHW shapes counts only the
+# two-phase slots).
 CASES = [
     dict(shape=(2, 64, 64, 320), cl=1, dtype=np.float16, mdtype=np.float32, skip="nc",
-         bias=True, groups=32, act=1, want_sum=True),
+         bias=True, groups=32, act=1, want_sum=True, route=2),
+    dict(shape=(4, 64, 64, 320), cl=1, dtype=np.float16, mdtype=np.float32, skip="full",
+         bias=True, groups=32, act=1, want_sum=True, route=6),
+    dict(shape=(2, 128, 128, 320), cl=1, dtype=np.float16, mdtype=np.float32, skip="nc",
+         bias=True, groups=32, act=0, want_sum=True, route=5),
     dict(shape=(16, 1280, 16, 16), cl=0, dtype=np.float32, mdtype=np.float16, skip="full",
          bias=False, groups=32, act=0, want_sum=False),
     dict(shape=(1, 64, 128, 128), cl=0, dtype=np.float16, mdtype=np.float32, skip="nc",
@@ -90,8 +96,16 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES,
-                         ids=["nhwc_coop", "nchw_resident", "nchw_two_phase", "nchw_64_groups"])
+                         ids=["nhwc_coop", "nhwc_slab", "nhwc_coop_l2", "nchw_resident",
+                              "nchw_two_phase", "nchw_64_groups"])
 def test_noalloc_matches_oracle_and_regular_entry_two_calls_in_a_row(case):
+    if "route" in case:  # the route the case is here for
+        N, H, W, C = case["shape"]
+        out = (ctypes.c_int64 * 8)()
+        assert b2.library().b200norm_testing_plan_group(
+            N, C, H, W, case["groups"], _CODE[np.dtype(case["dtype"])],
+            _CODE[np.dtype(case["mdtype"])], 1, 1, out) == 0
+        assert out[0] == case["route"]
     outs = []
     for seed in (101, 202):  # two calls in a row on the shared scratch
         d = synthetic.skip_group_inputs(case["shape"], case["dtype"], case["mdtype"], seed=seed,
