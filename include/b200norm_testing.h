@@ -80,6 +80,12 @@ B200NORM_API b200norm_status b200norm_testing_pipe_stall(int on, uint64_t limit_
 B200NORM_API b200norm_status b200norm_testing_plan_rows(int64_t rows, int64_t n,
                                                         b200norm_dtype T, int aligned16,
                                                         int64_t out[8]);
+/* The same for GatedRMSNorm spans of C elements (b200norm_testing_plan_rows
+ * gives SkipSimplifiedLayerNormalization's plan; the two differ for some
+ * widths when there are many rows). */
+B200NORM_API b200norm_status b200norm_testing_plan_gated(int64_t rows, int64_t C,
+                                                         b200norm_dtype T, int aligned16,
+                                                         int64_t out[8]);
 B200NORM_API b200norm_status b200norm_testing_plan_group(int64_t N, int64_t C, int64_t H,
                                                          int64_t W, int groups, b200norm_dtype T,
                                                          b200norm_dtype M, int channels_last,

@@ -90,6 +90,8 @@ def library() -> ctypes.CDLL:
             "b200norm_testing_pipe_stall": ([i32, ctypes.c_uint64], i32),
             "b200norm_testing_plan_rows": ([i64, i64, i32, i32, ctypes.POINTER(ctypes.c_int64)],
                                            i32),
+            "b200norm_testing_plan_gated": ([i64, i64, i32, i32, ctypes.POINTER(ctypes.c_int64)],
+                                            i32),
             "b200norm_testing_plan_group": ([i64, i64, i64, i64, i32, i32, i32, i32, i32,
                                              ctypes.POINTER(ctypes.c_int64)], i32),
         }

@@ -153,7 +153,7 @@ b200norm_status skip_rms_impl(const void* input, const void* skip, const void* g
   bool vec = hidden % ve == 0;
   for (const void* p : ptrs)
     if (p && !aligned(p, 16)) vec = false;
-  RowPlan plan = plan_rows(rows, hidden, to_dtype(T), vec);
+  RowPlan plan = plan_rows(rows, hidden, to_dtype(T), vec, RowOp::SkipRms);
   if (g_force_csize)
     if (b200norm_status st = forced_split(rows, hidden, &plan)) return st;
   if (g_force_row_mode == 0 && !g_force_csize)
@@ -310,7 +310,7 @@ b200norm_status b200norm_gated_rms(const void* x, const void* gate, const void* 
   bool vec = C % ve == 0;
   for (const void* p : ptrs)
     if (!aligned(p, 16)) vec = false;
-  RowPlan plan = plan_rows(rows, C, to_dtype(T), vec);
+  RowPlan plan = plan_rows(rows, C, to_dtype(T), vec, RowOp::Gated);
   if (g_force_csize)
     if (b200norm_status st = forced_split(rows, C, &plan)) return st;
   if (g_force_row_mode == 2) plan = forced_walk(rows, plan);
@@ -471,15 +471,25 @@ b200norm_status b200norm_testing_set_pdl(int on) {
   return ok();
 }
 
-b200norm_status b200norm_testing_plan_rows(int64_t rows, int64_t n, b200norm_dtype T,
-                                           int aligned16, int64_t out[8]) {
+static b200norm_status plan_rows_query(int64_t rows, int64_t n, b200norm_dtype T, int aligned16,
+                                       RowOp op, int64_t out[8]) {
   if (!dtype_ok(T) || n <= 0 || rows < 0 || !out)
     return fail(B200NORM_ERR_INVALID_ARGUMENT, "bad plan query");
   const int ve = static_cast<int>(16 / dtype_size(to_dtype(T)));
-  const RowPlan p = plan_rows(rows, n, to_dtype(T), aligned16 && n % ve == 0);
+  const RowPlan p = plan_rows(rows, n, to_dtype(T), aligned16 && n % ve == 0, op);
   const int64_t v[8] = {p.mode, p.ve, p.tpr, p.nv, p.rpg, p.block, p.csize, p.grid};
   for (int i = 0; i < 8; ++i) out[i] = v[i];
   return ok();
+}
+
+b200norm_status b200norm_testing_plan_rows(int64_t rows, int64_t n, b200norm_dtype T,
+                                           int aligned16, int64_t out[8]) {
+  return plan_rows_query(rows, n, T, aligned16, RowOp::SkipRms, out);
+}
+
+b200norm_status b200norm_testing_plan_gated(int64_t rows, int64_t C, b200norm_dtype T,
+                                            int aligned16, int64_t out[8]) {
+  return plan_rows_query(rows, C, T, aligned16, RowOp::Gated, out);
 }
 
 b200norm_status b200norm_testing_plan_group(int64_t N, int64_t C, int64_t H, int64_t W, int groups,

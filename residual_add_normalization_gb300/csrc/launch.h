@@ -103,8 +103,10 @@ inline unsigned add_pdl_attr(cudaLaunchAttribute* attrs, unsigned n) {
   return n + 1;
 }
 
-// Row plans depend only on the shape, element type and pointer alignment.
-RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok);
+// Row plans depend on the operator, the shape, the element type and the
+// pointer alignment.
+enum class RowOp { SkipRms, Gated };
+RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok, RowOp op);
 
 // The pipelined lane-group plan for spans of n elements, if the span takes
 // it (16-byte vectors, at most 32 of them); false otherwise.

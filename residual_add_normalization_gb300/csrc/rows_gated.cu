@@ -16,6 +16,22 @@
 // than 1024 vectors take 512 threads).  Splitting a row over a cluster only
 // pays once one CTA cannot hold it.
 constexpr int64_t kFewRows = 256;
+// Past kFewRows rows (measured on GB300 over widths of 512-16384 elements,
+// rows enough for two 512 MB buffer sets, CUDA-graph replay):
+//  - SkipSimplifiedLayerNormalization rows of 97-159 vectors go to one CTA
+//    per row rather than a warp per row: a warp holding four vectors of two
+//    inputs per lane runs at 125 registers, two 256-thread CTAs per SM, too
+//    few warps to hide its epilogue (hidden 1024 fp16: 77.2 us vs 87.7; 896:
+//    78.5 vs 83.0; at 96 vectors and fewer the warp stays ahead, 84.4 vs
+//    89.6 at 768);
+//  - a CTA row that is not a whole number of warps takes two vectors per
+//    thread (hidden 896: 78.5 vs 81.2 us; 1152: 77.9 vs 81.7);
+//  - GatedRMSNorm CTA rows take at least two vectors per thread (C = 1536 /
+//    2048 fp16: 78.2 / 78.2 us vs 87.9 / 87.1 with one; bf16 C = 2048 78.5 vs
+//    87.8; float32 C = 1024 76.5 vs 77.3); its rows of up to 128 vectors
+//    stay on a warp each (C = 1024 fp16: 86.1 us vs 90.1 for a CTA).
+constexpr int kSslnCtaFromVec = 97;
+constexpr int kSslnPairBelowVec = 160;
 
 namespace b200norm {
 
@@ -29,7 +45,7 @@ static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 static int round32(int64_t v) { return static_cast<int>(ceil_div(v, 32) * 32); }
 
-RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok) {
+RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok, RowOp op) {
   RowPlan p = {};
   p.ve = vector_ok ? static_cast<int>(16 / dtype_size(t)) : 1;
   const int64_t nvec = n / p.ve;
@@ -43,7 +59,8 @@ RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok) {
     p.rpg = p.nv == 1 && p.tpr <= 16 ? B200NORM_SHORT_RPG : 1;
     p.block = lane_block(p.nv * p.rpg);
     p.grid = ceil_div(rows, static_cast<int64_t>(p.block / p.tpr) * p.rpg);
-  } else if (nvec <= 128) {
+  } else if (nvec <= 128 &&
+             !(op == RowOp::SkipRms && rows > kFewRows && nvec >= kSslnCtaFromVec)) {
     // Warp per row, up to four vectors per lane.
     p.mode = 0;
     p.tpr = 32;
@@ -53,9 +70,12 @@ RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok) {
   } else {
     // CTA per row; a cluster per row once one CTA cannot hold it.
     p.mode = 1;
+    const bool many = rows > kFewRows;
     int nv = 1;
-    int cta = round32(nvec);
-    const int target = rows <= kFewRows ? kRowsMaxThreads : 256;
+    if (many && op == RowOp::Gated) nv = 2;
+    if (many && op == RowOp::SkipRms && nvec < kSslnPairBelowVec && nvec % 32 != 0) nv = 2;
+    int cta = round32(ceil_div(nvec, nv));
+    const int target = many ? 256 : kRowsMaxThreads;
     while (cta > target && nv < 4) {
       nv *= 2;
       cta = round32(ceil_div(nvec, nv));

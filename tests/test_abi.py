@@ -193,15 +193,16 @@ def test_noalloc_refuses_before_touching_a_device(lib):
     assert lib.b200norm_skip_group_workspace_size(2, 64, 8, 8, 64, F16, 1) > 256 + (2 << 20)
 
 
-def plan_rows(lib, rows, n, T, aligned=1):
+def plan_rows(lib, rows, n, T, aligned=1, gated=False):
     out = (ctypes.c_int64 * 8)()
-    assert lib.b200norm_testing_plan_rows(rows, n, T, aligned, out) == OK
+    fn = lib.b200norm_testing_plan_gated if gated else lib.b200norm_testing_plan_rows
+    assert fn(rows, n, T, aligned, out) == OK
     return dict(zip(("mode", "ve", "tpr", "nv", "rpg", "block", "csize", "grid"), out))
 
 
 def test_row_planner_shapes(lib):
     # GatedRMSNorm C = 128 fp16: 16 vectors of 8 -> 16-lane groups, 2 spans per warp
-    p = plan_rows(lib, 1 << 20, 128, F16)
+    p = plan_rows(lib, 1 << 20, 128, F16, gated=True)
     assert (p["mode"], p["ve"], p["tpr"]) == (0, 8, 16)
     assert p["grid"] * (p["block"] // p["tpr"]) * p["rpg"] >= 1 << 20
     # SSLN hidden 4096 fp16: CTA per row, every vector covered
@@ -214,6 +215,21 @@ def test_row_planner_shapes(lib):
     assert (plan_rows(lib, 16384, 4096, F16)["nv"], plan_rows(lib, 16384, 4096, F16)["block"]) == (2, 256)
     assert (plan_rows(lib, 16384, 4096, F32)["nv"], plan_rows(lib, 16384, 4096, F32)["block"]) == (4, 256)
     assert (plan_rows(lib, 16384, 8192, F32)["nv"], plan_rows(lib, 16384, 8192, F32)["block"]) == (4, 512)
+    # many rows (measured): SSLN rows of 97-159 vectors on a CTA each, two
+    # vectors per thread unless the row is a whole number of warps; GatedRMSNorm
+    # CTA rows with at least two vectors per thread, rows of up to 128 vectors
+    # on a warp each
+    for n, T, want in ((768, F16, (0, 4)), (896, F16, (1, 2)), (1024, F16, (1, 1)),
+                       (1152, F16, (1, 2)), (1280, F16, (1, 1)), (512, F32, (1, 1))):
+        p = plan_rows(lib, 65536, n, T)
+        assert (p["mode"], p["nv"]) == want, (n, T, p)
+    for n, T, want in ((1024, F16, (0, 4)), (1536, F16, (1, 2)), (2048, F16, (1, 2)),
+                       (8192, F16, (1, 4)), (1024, F32, (1, 2))):
+        p = plan_rows(lib, 65536, n, T, gated=True)
+        assert (p["mode"], p["nv"]) == want, (n, T, p)
+    # ... but few rows keep the latency-bound choice
+    assert plan_rows(lib, 64, 1024, F16)["mode"] == 0
+    assert plan_rows(lib, 64, 2048, F16, gated=True)["nv"] == 1
     # odd hidden: scalar path
     p = plan_rows(lib, 3, 5, F32)
     assert p["ve"] == 1 and p["tpr"] >= 5
@@ -224,10 +240,12 @@ def test_row_planner_shapes(lib):
     assert p["mode"] == 1 and p["csize"] >= 2 and p["tpr"] * p["nv"] * p["ve"] >= 65536
     assert plan_rows(lib, 1, 1 << 24, F16)["mode"] == 2
     # every plan covers the row
-    for n in (1, 3, 8, 24, 100, 256, 257, 768, 1000, 4096, 12288, 40000, 300000):
+    for n, rows, gated in [(n, r, g) for n in (1, 3, 8, 24, 100, 256, 257, 768, 896, 1000, 1152,
+                                                4096, 12288, 40000, 300000)
+                           for r in (5, 65536) for g in (False, True)]:
         for T in (F32, F16):
             for al in (0, 1):
-                p = plan_rows(lib, 5, n, T, al)
+                p = plan_rows(lib, rows, n, T, al, gated)
                 nvec = n // p["ve"]
                 assert n % p["ve"] == 0
                 if p["mode"] != 2:
