@@ -8,30 +8,38 @@
 #ifndef B200NORM_SHORT_NV
 #define B200NORM_SHORT_NV 1    // vectors per thread for spans of <= 32 vectors
 #endif
-// CTA-per-row schedules.  Measured on GB300 (fp16 / fp32 rows of 4096 and
-// 8192 elements, CUDA-graph replay): with up to kFewRows rows the call is
-// latency-bound and the widest CTA (fewest vectors per thread, up to 512
-// threads) is fastest -- 1.7 us instead of 2.8 us for one fp16 row of 4096;
-// with more rows CTAs of about 256 threads are (nv capped at 4; rows of more
-// than 1024 vectors take 512 threads).  Splitting a row over a cluster only
-// pays once one CTA cannot hold it.
-constexpr int64_t kFewRows = 256;
-// Past kFewRows rows (measured on GB300 over widths of 512-16384 elements,
-// rows enough for two 512 MB buffer sets, CUDA-graph replay):
-//  - SkipSimplifiedLayerNormalization rows of 97-159 vectors go to one CTA
-//    per row rather than a warp per row: a warp holding four vectors of two
-//    inputs per lane runs at 125 registers, two 256-thread CTAs per SM, too
-//    few warps to hide its epilogue (hidden 1024 fp16: 77.2 us vs 87.7; 896:
-//    78.5 vs 83.0; at 96 vectors and fewer the warp stays ahead, 84.4 vs
-//    89.6 at 768);
-//  - a CTA row that is not a whole number of warps takes two vectors per
-//    thread (hidden 896: 78.5 vs 81.2 us; 1152: 77.9 vs 81.7);
-//  - GatedRMSNorm CTA rows take at least two vectors per thread (C = 1536 /
-//    2048 fp16: 78.2 / 78.2 us vs 87.9 / 87.1 with one; bf16 C = 2048 78.5 vs
-//    87.8; float32 C = 1024 76.5 vs 77.3); its rows of up to 128 vectors
-//    stay on a warp each (C = 1024 fp16: 86.1 us vs 90.1 for a CTA).
+// CTA-per-row schedules, measured on GB300 (CUDA-graph replay, inputs from
+// HBM; widths of 512-16384 elements, 128 rows to 512 MB per call):
+//  - up to kFewRows rows the call is latency-bound and the widest CTA (fewest
+//    vectors per thread, up to 512 threads) is fastest or within 2% -- 1.7 us
+//    instead of 2.8 for one fp16 row of 4096; at 512 rows of 4096 GatedRMSNorm
+//    4.21 us vs 4.44 with 256 threads;
+//  - with more rows, CTAs of about 256 threads (nv capped at 4; rows of more
+//    than 1024 vectors take 512 threads), except that 16-bit SkipSimplified-
+//    LayerNormalization rows of 1024 vectors and more take up to 512 threads
+//    with two vectors each (hidden 8192 fp16: 12.5 us vs 13.7 at 1024 rows,
+//    78.3 vs 78.8 at 8192; bf16 78.4 vs 78.9 at 8192), while float32 rows of
+//    1024 vectors keep 256 threads of four (hidden 4096: 41.1 us vs 48.1 at
+//    4096 rows);
+//  - SkipSimplifiedLayerNormalization rows of 97-128 vectors go to a CTA, not
+//    a warp, past kSslnCtaRows rows: the warp, holding four vectors of two
+//    inputs per lane, runs at 125 registers, two 256-thread CTAs per SM, too
+//    few warps to hide its epilogue (hidden 1024 fp16: 2.49 us vs 3.04 at 512
+//    rows, 20.9 vs 22.6 at 16 K rows, 77.1 vs 87.7 at 64 K); at 96 vectors and
+//    fewer the warp stays ahead (84.4 vs 89.6 us at 768, 64 K rows);
+//  - from kPairRows rows, GatedRMSNorm CTA rows and SkipSimplifiedLayer-
+//    Normalization CTA rows of fewer than 160 vectors that are not a whole
+//    number of warps take two vectors per thread (GatedRMSNorm C = 2048 fp16:
+//    59.8 us vs 65.3 at 32 K rows, 78.2 vs 87.1 at 43 K; hidden 1152 fp16:
+//    23.8 vs 24.6 at 16 K); below it one vector per thread is faster (C = 2048:
+//    4.0 us vs 4.2 at 1 K rows; hidden 1152: 2.6 vs 2.9 at 512).
+// Splitting a row over a cluster only pays once one CTA cannot hold it.
+constexpr int64_t kFewRows = 512;
+constexpr int64_t kSslnCtaRows = 256;
+constexpr int64_t kPairRows = 8192;
 constexpr int kSslnCtaFromVec = 97;
 constexpr int kSslnPairBelowVec = 160;
+constexpr int kSslnWideFromVec = 1024;
 
 namespace b200norm {
 
@@ -60,7 +68,7 @@ RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok, RowOp op) {
     p.block = lane_block(p.nv * p.rpg);
     p.grid = ceil_div(rows, static_cast<int64_t>(p.block / p.tpr) * p.rpg);
   } else if (nvec <= 128 &&
-             !(op == RowOp::SkipRms && rows > kFewRows && nvec >= kSslnCtaFromVec)) {
+             !(op == RowOp::SkipRms && rows > kSslnCtaRows && nvec >= kSslnCtaFromVec)) {
     // Warp per row, up to four vectors per lane.
     p.mode = 0;
     p.tpr = 32;
@@ -70,12 +78,15 @@ RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok, RowOp op) {
   } else {
     // CTA per row; a cluster per row once one CTA cannot hold it.
     p.mode = 1;
-    const bool many = rows > kFewRows;
     int nv = 1;
-    if (many && op == RowOp::Gated) nv = 2;
-    if (many && op == RowOp::SkipRms && nvec < kSslnPairBelowVec && nvec % 32 != 0) nv = 2;
+    if (rows >= kPairRows &&
+        (op == RowOp::Gated || (nvec < kSslnPairBelowVec && nvec % 32 != 0)))
+      nv = 2;
     int cta = round32(ceil_div(nvec, nv));
-    const int target = many ? 256 : kRowsMaxThreads;
+    const int target = rows <= kFewRows ? kRowsMaxThreads
+                       : (op == RowOp::SkipRms && t != DType::F32 && nvec >= kSslnWideFromVec)
+                           ? kRowsMaxThreads
+                           : 256;
     while (cta > target && nv < 4) {
       nv *= 2;
       cta = round32(ceil_div(nvec, nv));

@@ -223,13 +223,20 @@ def test_row_planner_shapes(lib):
                        (1152, F16, (1, 2)), (1280, F16, (1, 1)), (512, F32, (1, 1))):
         p = plan_rows(lib, 65536, n, T)
         assert (p["mode"], p["nv"]) == want, (n, T, p)
+    # ... two vectors per thread only from 8,192 rows; 16-bit SSLN rows of 1,024
+    # vectors in 512-thread CTAs (float32 keeps 256 threads of four)
+    assert plan_rows(lib, 4096, 1152, F16)["nv"] == 1
+    assert plan_rows(lib, 4096, 2048, F16, gated=True)["nv"] == 1
+    assert (plan_rows(lib, 4096, 8192, F16)["nv"], plan_rows(lib, 4096, 8192, F16)["block"]) == (2, 512)
+    assert (plan_rows(lib, 4096, 4096, F32)["nv"], plan_rows(lib, 4096, 4096, F32)["block"]) == (4, 256)
     for n, T, want in ((1024, F16, (0, 4)), (1536, F16, (1, 2)), (2048, F16, (1, 2)),
                        (8192, F16, (1, 4)), (1024, F32, (1, 2))):
         p = plan_rows(lib, 65536, n, T, gated=True)
         assert (p["mode"], p["nv"]) == want, (n, T, p)
-    # ... but few rows keep the latency-bound choice
+    # ... but few rows keep the latency-bound choice (the widest CTA up to 512 rows)
     assert plan_rows(lib, 64, 1024, F16)["mode"] == 0
     assert plan_rows(lib, 64, 2048, F16, gated=True)["nv"] == 1
+    assert (plan_rows(lib, 512, 4096, F16)["nv"], plan_rows(lib, 512, 4096, F16)["block"]) == (1, 512)
     # odd hidden: scalar path
     p = plan_rows(lib, 3, 5, F32)
     assert p["ve"] == 1 and p["tpr"] >= 5
