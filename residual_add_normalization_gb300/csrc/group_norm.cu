@@ -376,14 +376,22 @@ static cudaError_t plan_group_uncached(const SkipGroupCall& c, bool vector_ok, i
     // Route 1: each CTA stages at most ~40 KB of S in shared memory (five
     // such CTAs fit an SM), so an instance takes ceil(bytes / 40 KB) CTAs of
     // a cluster (at most 16); small instances under-filling the GPU are split
-    // further while each CTA keeps at least two vectors per thread.
+    // further while each CTA keeps at least two vectors per thread, or one
+    // while the cluster stays at most 4 and the grid within 2 x SMs.
+    // (Measured on GB300, fp16, SiLU, inputs from HBM: (2, 1280, 16, 16)
+    // 4.72 us with clusters of 4 vs 5.30 with 2; (1, 1280, 16, 16) 4.23 vs
+    // 5.07; (2, 320, 32, 32) 4.72 vs 5.29; but (2, 640, 32, 32) 6.84 with 8
+    // vs 6.15 with 4, and (4, 1280, 16, 16) 6.59 with 512 CTAs vs 6.08.)
     const int ve = (vector_ok && HW % vec_elems == 0) ? vec_elems : 1;
     const int64_t nvec = L / ve;
     const int64_t vbytes = static_cast<int64_t>(ve) * static_cast<int64_t>(dtype_size(c.t));
     const int64_t insts = c.N * c.groups;
     const int64_t target = B200NORM_NCHW_TARGET_KB * 1024;
     int64_t cs = cdiv(nvec * vbytes, target);
-    while (cs < 16 && insts * cs < 2LL * sms && cdiv(nvec, cs * 2) >= 2LL * kNchwThreads) cs *= 2;
+    while (cs < 16 && insts * cs < 2LL * sms &&
+           (cdiv(nvec, cs * 2) >= 2LL * kNchwThreads ||
+            (cs < 4 && insts * cs * 2 <= 2LL * sms && cdiv(nvec, cs * 2) >= kNchwThreads)))
+      cs *= 2;
     if (cs > 16 || L > 0x7fffffffLL) {
       *p = two_phase_plan(c);
       return cudaSuccess;
