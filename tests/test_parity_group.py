@@ -164,6 +164,12 @@ def test_route_coverage():
     # else the cooperative route with the slabs in shared memory, else one
     # cooperative grid through L2.  (The plan query assumes a full-shape skip,
     # whose slab in shared memory doubles that of X.)
+    # small NCHW batches: instances split over clusters while the grid stays
+    # within 2 x SMs (measured faster), not beyond
+    for shape, cs in (((2, 1280, 16, 16), 4), ((1, 1280, 16, 16), 4), ((4, 1280, 16, 16), 2),
+                      ((2, 640, 32, 32), 4)):
+        p = plan(shape, 32, np.float16, np.float32, 0)
+        assert (p["route"], p["csize"]) == (1, cs), (shape, p)
     assert plan((2, 64, 64, 320), 32, np.float16, np.float32, 1)["route"] == 2
     assert plan((64, 8, 8, 64), 8, np.float16, np.float32, 1)["route"] == 2
     assert plan((4, 64, 64, 320), 32, np.float16, np.float32, 1)["route"] == 6
