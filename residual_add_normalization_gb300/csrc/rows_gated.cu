@@ -27,12 +27,14 @@
 //    few warps to hide its epilogue (hidden 1024 fp16: 2.49 us vs 3.04 at 512
 //    rows, 20.9 vs 22.6 at 16 K rows, 77.1 vs 87.7 at 64 K); at 96 vectors and
 //    fewer the warp stays ahead (84.4 vs 89.6 us at 768, 64 K rows);
-//  - from kPairRows rows, GatedRMSNorm CTA rows and SkipSimplifiedLayer-
-//    Normalization CTA rows of fewer than 160 vectors that are not a whole
-//    number of warps take two vectors per thread (GatedRMSNorm C = 2048 fp16:
-//    59.8 us vs 65.3 at 32 K rows, 78.2 vs 87.1 at 43 K; hidden 1152 fp16:
-//    23.8 vs 24.6 at 16 K); below it one vector per thread is faster (C = 2048:
-//    4.0 us vs 4.2 at 1 K rows; hidden 1152: 2.6 vs 2.9 at 512).
+//  - from kPairRows rows, GatedRMSNorm CTA rows and 16-bit SkipSimplified-
+//    LayerNormalization CTA rows of fewer than 160 vectors that are not a
+//    whole number of warps take two vectors per thread (GatedRMSNorm C = 2048
+//    fp16: 59.8 us vs 65.3 at 32 K rows, 78.2 vs 87.1 at 43 K; hidden 1152
+//    fp16: 23.8 vs 24.6 at 16 K); below it one vector per thread is faster
+//    (C = 2048: 4.0 us vs 4.2 at 1 K rows; hidden 1152: 2.6 vs 2.9 at 512),
+//    and so it is for float32 SkipSimplifiedLayerNormalization rows at any
+//    count (hidden 448: 68.3 us vs 71.6, 576: 85.8 vs 97.0 at 64 K rows).
 // Splitting a row over a cluster only pays once one CTA cannot hold it.
 constexpr int64_t kFewRows = 512;
 constexpr int64_t kSslnCtaRows = 256;
@@ -80,7 +82,8 @@ RowPlan plan_rows(int64_t rows, int64_t n, DType t, bool vector_ok, RowOp op) {
     p.mode = 1;
     int nv = 1;
     if (rows >= kPairRows &&
-        (op == RowOp::Gated || (nvec < kSslnPairBelowVec && nvec % 32 != 0)))
+        (op == RowOp::Gated ||
+         (t != DType::F32 && nvec < kSslnPairBelowVec && nvec % 32 != 0)))
       nv = 2;
     int cta = round32(ceil_div(nvec, nv));
     const int target = rows <= kFewRows ? kRowsMaxThreads

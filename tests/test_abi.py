@@ -220,7 +220,8 @@ def test_row_planner_shapes(lib):
     # CTA rows with at least two vectors per thread, rows of up to 128 vectors
     # on a warp each
     for n, T, want in ((768, F16, (0, 4)), (896, F16, (1, 2)), (1024, F16, (1, 1)),
-                       (1152, F16, (1, 2)), (1280, F16, (1, 1)), (512, F32, (1, 1))):
+                       (1152, F16, (1, 2)), (1280, F16, (1, 1)), (512, F32, (1, 1)),
+                       (448, F32, (1, 1)), (576, F32, (1, 1))):
         p = plan_rows(lib, 65536, n, T)
         assert (p["mode"], p["nv"]) == want, (n, T, p)
     # ... two vectors per thread only from 8,192 rows; 16-bit SSLN rows of 1,024
